@@ -1,0 +1,478 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized-weight matmul on GB300.
+
+Default workload (one "step"): the decode GEMV at nt = 1 on two Llama-7B-shaped
+Q4_K projections, od x K = 4096 x 4096 and 11008 x 4096, with x ~ N(0, 1) plus
+0.1% outliers x20.  A step runs the whole path for both: q8_1 quantization of
+x, then the MMVQ kernel (the nt <= 8 branch of the dispatch), through the C ABI.
+
+value   weight GB/s of the whole job: weight bytes of all steps on all ranks /
+        max-over-ranks wall time of the timed region, inputs resident in HBM.
+        Each step reads the next of 16 rotating weight copies (557 MB > 4x L2),
+        so no step finds its weights in L2.  The steps are replayed as one
+        CUDA graph per copy.
+e2e     the same metric with the activations copied from pinned host memory and
+        the outputs copied back inside every step, one qmm_matmul call per
+        projection from Python.
+roofline  the MMVQ kernel alone on the 11008 x 4096 projection: algorithmic bytes
+        (weights + q8_1 activations + f32 outputs) per launch / its mean launch
+        time (CUDA events around back-to-back launches over rotating copies),
+        against the measured HBM copy bandwidth.
+cpu_baseline  the CPU oracle (plain scalar C, all host cores) on the same step.
+
+--impl reference   times the CPU oracle alone as the reference arm.
+--sweep            one JSON line per case of every workload family (kernel-only
+                   timings and roofline fractions); not the contract line.
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run, one rank per GPU, each rank running the same workload on
+its own GPU (replicas; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q4_K×q8_1 matmul TOPS & weight GB/s vs nt (1..512), % of HBM/int8 roofline"
+WORKLOAD = "decode_gemv_q4k"
+NCOPIES = 16
+
+# ncu capture of the MMVQ kernel (nt = 1, 11008 x 4096): dram read + write bytes
+# per launch, and the hash of qmm_gemv.cu it was taken on.  Reported as
+# roofline.traffic only while the kernel source is unchanged.
+NCU_TRAFFIC = {"source_sha1": None, "bytes_per_launch": None}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def source_sha1(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------- clocks ------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.2)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ oracle -----
+def time_oracle(cases, budget_s: float, threads: int):
+    """Run whole oracle steps (quantize + matmul of every case) until the time
+    budget is spent; return (seconds per step, steps)."""
+    import oracle
+    ora = oracle.Oracle()
+    data = [c.generate() for c in cases]
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        for c, (W, x) in zip(cases, data):
+            ora.matmul(c.qtype, W, x, c.od, nthreads=threads)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s and steps >= 1:
+            return el / steps, steps
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------- main ------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def max_over_ranks(value: float, world: int, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm.  Each step is a bounded sample of
+    the workload -- a rotating contiguous block of rows of each projection,
+    sized so that warm-up plus timed steps take about `--ref-seconds` -- and
+    the value is weight bytes actually processed per second."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from quantized_weight_matmul_gb300 import synth
+    cases = synth.WORKLOADS[WORKLOAD].cases
+    cores = cpu_cores()
+    ora = oracle.Oracle()
+    data = [c.generate() for c in cases]
+    t0 = time.perf_counter()
+    for c, (W, x) in zip(cases, data):
+        ora.matmul(c.qtype, W, x, c.od, nthreads=cores)
+    t_full = time.perf_counter() - t0
+    frac = min(1.0, args.ref_seconds / max(1, args.steps + args.warmup) / max(t_full, 1e-9))
+    nrows = [max(1, int(c.od * frac)) for c in cases]
+    starts = [0] * len(cases)
+
+    def one_step():
+        done_bytes = done_macs = 0
+        for i, (c, (W, x)) in enumerate(zip(cases, data)):
+            r0 = starts[i]
+            r1 = min(c.od, r0 + nrows[i])
+            ora.matmul(c.qtype, np.ascontiguousarray(W[r0:r1]), x, r1 - r0, nthreads=cores)
+            done_bytes += (r1 - r0) * (c.K // 256) * synth.BLOCK_BYTES[c.qtype]
+            done_macs += (r1 - r0) * c.K * c.nt
+            starts[i] = 0 if r1 >= c.od else r1
+        return done_bytes, done_macs
+
+    for _ in range(args.warmup):
+        one_step()
+    tot_b = tot_m = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        b, m = one_step()
+        tot_b += b
+        tot_m += m
+    t = time.perf_counter() - t0
+    value = tot_b / t / 1e9
+    sample = (f"{nrows[0]} of {cases[0].od} and {nrows[1]} of {cases[1].od} rows per step "
+              f"(rotating row blocks; quantize + matmul)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 dots, f64 sums",
+        "data": "synthetic", "tops": 2 * tot_m / t / 1e12,
+        "config": {"workload": WORKLOAD, "shapes": [[c.od, c.K] for c in cases], "nt": 1, "qtype": "Q4_K",
+                   "x": "N(0,1) + 0.1% x20 outliers", "seed": 0},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "cpu": cpu_model(), "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import quantized_weight_matmul_gb300 as qmm
+    from quantized_weight_matmul_gb300 import synth
+
+    qmm.load()
+    peaks = load_peaks()
+    cases = synth.WORKLOADS[WORKLOAD].cases
+    stream = torch.cuda.Stream(device=dev)
+    st = stream.cuda_stream
+
+    host = [c.generate() for c in cases]
+    Wcopies = [[torch.from_numpy(W).to(dev) for _ in range(NCOPIES)] for (W, _) in host]
+    xs = [torch.from_numpy(x).to(dev) for (_, x) in host]
+    xqs = [torch.empty((c.nt, c.K), dtype=torch.int8, device=dev) for c in cases]
+    xdss = [torch.empty((c.nt, c.K // 32, 2), dtype=torch.float32, device=dev) for c in cases]
+    outs = [torch.empty((c.nt, c.od), dtype=torch.float32, device=dev) for c in cases]
+    wbytes = sum(c.weight_bytes for c in cases)
+    macs = sum(c.macs for c in cases)
+    launches_per_step = 2 * len(cases)  # quantize + MMVQ per projection
+
+    def step(copy, s=st):
+        for i, c in enumerate(cases):
+            rc = qmm.qmm_matmul(c.qtype, Wcopies[i][copy].data_ptr(), xs[i].data_ptr(), xqs[i].data_ptr(),
+                                xdss[i].data_ptr(), outs[i].data_ptr(), c.od, c.K, c.nt, 0, 0, s)
+            if rc != qmm.QMM_OK:
+                raise qmm.QmmError(rc, "qmm_matmul")
+
+    # warm up eagerly once (first-call set-up happens outside any capture), then capture
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    graphs = []
+    for k in range(NCOPIES):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(k, torch.cuda.current_stream().cuda_stream)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    assert qmm.qmm_sync_status(st) == qmm.QMM_OK
+
+    with torch.cuda.stream(stream):
+        for w in range(args.warmup):
+            graphs[w % NCOPIES].replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for s in range(args.steps):
+                graphs[s % NCOPIES].replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world, dev)
+    value = world * wbytes * args.steps / (ms_max / 1e3) / 1e9
+    tops = world * 2 * macs * args.steps / (ms_max / 1e3) / 1e12
+    clocks = clk.summary()
+    assert qmm.qmm_sync_status(st) == qmm.QMM_OK
+
+    # ---- roofline: the MMVQ kernel alone on the largest projection
+    big = max(range(len(cases)), key=lambda i: cases[i].weight_bytes)
+    c = cases[big]
+    nrep = 64 * NCOPIES
+    with torch.cuda.stream(stream):
+        for k in range(NCOPIES):
+            qmm.qmm_gemv(c.qtype, Wcopies[big][k].data_ptr(), xqs[big].data_ptr(), xdss[big].data_ptr(),
+                         outs[big].data_ptr(), c.od, c.K, c.nt, st)
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        for k in range(nrep):
+            qmm.qmm_gemv(c.qtype, Wcopies[big][k % NCOPIES].data_ptr(), xqs[big].data_ptr(),
+                         xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K, c.nt, st)
+        k1.record(stream)
+    torch.cuda.synchronize()
+    kernel_ms = k0.elapsed_time(k1) / nrep
+    alg_bytes = c.weight_bytes + c.nt * c.K + c.nt * (c.K // 32) * 8 + c.nt * c.od * 4
+    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    traffic = (NCU_TRAFFIC["bytes_per_launch"]
+               if NCU_TRAFFIC["source_sha1"] == source_sha1("quantized_weight_matmul_gb300/csrc/qmm_gemv.cu")
+               else None)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "kernel": "gemv_q4k_kernel<1> (MMVQ)", "shape": [c.od, c.K], "kernel_us": kernel_ms * 1e3,
+                "alg_bytes_per_launch": alg_bytes, "peak_source": peaks["source"] + " hbm_gbs (copy)"}
+
+    # ---- e2e: host activations in, host outputs back, one C-ABI call per projection
+    xh = [torch.from_numpy(x).pin_memory() for (_, x) in host]
+    oh = [torch.empty((cc.nt, cc.od), dtype=torch.float32).pin_memory() for cc in cases]
+    e2e_steps = max(1, min(args.steps, 2000))
+    with torch.cuda.stream(stream):
+        for s in range(e2e_steps + 5):
+            if s == 5:
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            for i, cc in enumerate(cases):
+                xs[i].copy_(xh[i], non_blocking=True)
+                rc = qmm.qmm_matmul(cc.qtype, Wcopies[i][s % NCOPIES].data_ptr(), xs[i].data_ptr(),
+                                    xqs[i].data_ptr(), xdss[i].data_ptr(), outs[i].data_ptr(), cc.od, cc.K,
+                                    cc.nt, 0, 0, st)
+                assert rc == qmm.QMM_OK
+                oh[i].copy_(outs[i], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e = {"value": world * wbytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": sum(cc.nt * cc.K * 4 for cc in cases),
+           "d2h_bytes_per_step": sum(cc.nt * cc.od * 4 for cc in cases), "ms_per_step": e2e_ms}
+
+    # ---- CPU baseline: the oracle on this host's cores (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = cpu_cores()
+        sec, nsteps = time_oracle(cases, args.cpu_seconds, cores)
+        cpu = {"value": wbytes / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "cpu": cpu_model(),
+               "sample": f"{nsteps} whole steps (both projections, quantize + matmul), {args.cpu_seconds:.0f} s budget"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8 dots (dp4a), f32 rescale",
+            "data": "synthetic", "tops": tops,
+            "config": {"workload": WORKLOAD, "shapes": [[cc.od, cc.K] for cc in cases], "nt": 1,
+                       "qtype": "Q4_K", "x": "N(0,1) + 0.1% x20 outliers", "seed": 0,
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"{NCOPIES} rotating weight copies ({NCOPIES * wbytes / 1e6:.0f} MB > L2)",
+                       "graphs": "one CUDA graph per step"},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_sweep(args):
+    """Kernel-only timing of every case of every workload family."""
+    import torch
+    import quantized_weight_matmul_gb300 as qmm
+    from quantized_weight_matmul_gb300 import synth
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    st = stream.cuda_stream
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    names = args.families.split(",") if args.families else list(synth.WORKLOADS)
+    for fam in names:
+        for c in synth.WORKLOADS[fam].cases:
+            W, x = c.generate()
+            ncopy = max(2, min(32, int(4 * l2 // c.weight_bytes) + 1))
+            Ws = [torch.from_numpy(W).to(dev) for _ in range(ncopy)]
+            xd = torch.from_numpy(x).to(dev)
+            xq, xds = qmm.quantize_q8_1(xd)
+            out = torch.empty((c.nt, c.od), dtype=torch.float32, device=dev)
+            use_gemv = c.qtype == qmm.Q4_K and c.nt <= 8
+            need = qmm.qmm_gemm_workspace_bytes(c.qtype, c.od, c.K, c.nt)
+            ws = qmm.workspace(need, dev)
+            xh = ws.view(torch.uint8)
+
+            def launch(k):
+                if use_gemv:
+                    return qmm.qmm_gemv(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
+                                        c.od, c.K, c.nt, st)
+                return qmm.qmm_gemm(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
+                                    c.od, c.K, c.nt, xh.data_ptr(), need, st)
+
+            reps = max(ncopy, int(min(2000, 2e11 / max(c.macs, 1))))
+            with torch.cuda.stream(stream):
+                for k in range(ncopy):
+                    assert launch(k) == 0
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for k in range(reps):
+                    launch(k % ncopy)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            assert qmm.qmm_sync_status(st) == 0
+            us = e0.elapsed_time(e1) / reps * 1e3
+            alg = c.weight_bytes + c.nt * c.K * 1.25 + c.nt * c.od * 4
+            tops = 2 * c.macs / (us / 1e6) / 1e12
+            rec = {"case": c.name, "path": "mmvq" if use_gemv else "mmq-tcgen05", "us": us,
+                   "weight_GBs": c.weight_bytes / (us / 1e6) / 1e9, "TOPS": tops,
+                   "hbm_frac": alg / (us / 1e6) / 1e9 / peaks["hbm_gbs"],
+                   "tensor_frac_f16": tops / peaks["bf16_tflops"], "copies": ncopy, "reps": reps,
+                   "note": "gemm time includes its activation prepass" if not use_gemv else ""}
+            print(json.dumps(rec), flush=True)
+            del Ws, ws
+            torch.cuda.empty_cache()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--families", default="")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,171 @@
+/*
+ * qmm.h -- C ABI of the GB300 (sm_103a) quantized-weight matmul library.
+ *
+ *     out[t][r] = sum_k W[r][k] * x[t][k]        t < nt, r < od, k < K
+ *
+ * W is kept as raw GGUF K-quant super-blocks (never dequantized to a float
+ * copy); the activations are quantized on the device to q8_1 blocks and the
+ * products are exact integer dots rescaled in fp32.
+ *
+ * Sources (page titles and sections):
+ *   [MMQ]  "llama.cpp MMQ -- quantized-weight int8 tensor-core matmul":
+ *          sec. 4 (Q4_K and Q6_K block layouts), sec. 6 (the (scale, min)
+ *          unpack, the rescale sum += dA*dB*C + mA*sB), sec. 12 (MMVQ keeps
+ *          up to 8 tokens in registers; MMQ beyond).
+ *   [MOJO] mojo-dllm "The quantized GEMM": "The GPU path" (warp-per-32 q8_1
+ *          quantizer with f32 scale and scale*sum(q); the identity
+ *          sum w x = d*sc*dx*sum(q*qx) - dmin*m*(dx*sum(qx)); one MMA per
+ *          scale group), "Weights" (zero points off the inner loop).
+ *   [CH04] "04 - Reading minfer's kernels II": sec. 2.2 (W row-major
+ *          [out][in], activations token-major [nt][in], out [nt][od]),
+ *          sec. 3.3 (errors, not silent fallbacks), sec. 3.4 (MMVQ).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named "device" are CUDA device pointers owned by the caller;
+ *     the library never frees, keeps or allocates device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; no call synchronizes the
+ *     host except qmm_sync_status.
+ *   - Layouts: W is row-major [od][K/256] super-blocks (raw GGUF bytes,
+ *     16-byte aligned base); x and xq are token-major [nt][K]; xds is
+ *     [nt][K/32][2] f32 = (d, s); out is [nt][od] f32, od contiguous.
+ *   - Preconditions checked on the host: qtype is QMM_Q4_K or QMM_Q6_K;
+ *     K > 0 and K % 256 == 0; od >= 1; nt >= 1 (qmm_gemv: 1 <= nt <= 8);
+ *     od, K, nt and od*nt, nt*K below 2^31; non-NULL pointers; W, x, xq,
+ *     xds, out and the workspace 16-byte aligned.  Inputs must be finite.
+ *   - Every call returns QMM_OK (0) or a negative QMM_E* code and launches
+ *     nothing when it fails a check.  There is no fallback to another kernel,
+ *     to the CPU or to a dense library GEMM.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight block types.  12 is the GGML id of Q4_K ([MMQ] sec. 1); 14 is the
+ * public GGML id of Q6_K. */
+typedef enum { QMM_Q4_K = 12, QMM_Q6_K = 14 } qmm_qtype;
+
+enum {
+    QMM_OK = 0,
+    QMM_EINVAL_QTYPE = -1, /* qtype is not QMM_Q4_K / QMM_Q6_K            */
+    QMM_EINVAL_SHAPE = -2, /* od, K or nt out of range                    */
+    QMM_EALIGN = -3,       /* a pointer is not 16-byte aligned            */
+    QMM_ENULL = -4,        /* a required pointer is NULL                  */
+    QMM_EWORKSPACE = -5,   /* workspace smaller than required             */
+    QMM_ESMEM = -6,        /* the kernel's shared memory exceeds the cap  */
+    QMM_ELAUNCH = -7,      /* a CUDA runtime call or launch failed        */
+    QMM_ETIMEOUT = -8,     /* a bounded device-side wait gave up          */
+    QMM_EDEVICE = -9,      /* no usable sm_103 device is current          */
+};
+
+/* ------------------------------------------------------------ sizes ---- */
+
+/* Bytes of W [od][K] in `qtype`: od*K/256*144 (Q4_K) or od*K/256*210
+ * (Q6_K) ([MMQ] sec. 4).  0 for an invalid qtype or shape.  Host only. */
+size_t qmm_weight_bytes(int qtype, int64_t od, int64_t K);
+
+/* Bytes of the q8_1 activations: xq = nt*K int8, xds = nt*(K/32)*2 f32. */
+size_t qmm_xq_bytes(int64_t nt, int64_t K);
+size_t qmm_xds_bytes(int64_t nt, int64_t K);
+
+/* Workspace qmm_gemm needs for this problem (f16 copy of the int8 codes and
+ * token-contiguous scale planes, see qmm_gemm).  0 for invalid input. */
+size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
+
+/* Workspace qmm_matmul needs: qmm_gemm_workspace_bytes when nt > 8, else 0. */
+size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
+
+/* Largest nt qmm_gemv accepts (8, the register token loop of [MMQ] sec. 12). */
+int qmm_gemv_max_nt(void);
+
+/* ------------------------------------------------------- device work ---- */
+
+/*
+ * q8_1 quantization of x [nt][K] f32 ([MOJO] "The GPU path"; [CH04]
+ * sec. 3.4).  One warp per 32-value block, one value per lane: amax by a
+ * shuffle max, d = amax/127 (IEEE f32 division), q = round-half-even(x/d)
+ * clamped to [-127, 127], s = d * (float)sum(q) with sum(q) an integer
+ * shuffle sum.  A block of zeros gives d = s = 0 and q = 0.
+ * Output: xq [nt][K] int8, xds [nt][K/32][2] f32 (d, s).  K % 32 == 0
+ * suffices here.  Bit-exact with the IEEE definition.
+ */
+int qmm_quantize_q8_1(const float *x, int64_t nt, int64_t K, int8_t *xq, float *xds,
+                      void *stream);
+
+/*
+ * MMVQ: small-batch matmul for 1 <= nt <= 8 ([CH04] sec. 3.4; [MMQ] sec. 12).
+ * Streams every weight row once with 16-byte loads and keeps all nt tokens in
+ * registers, so the weight traffic does not grow with nt.  Per 32-value
+ * sub-block j (Q4_K) the integer dot D = sum(nibble * q) is rescaled as
+ * d*sc_j*dx*D - dmin*m_j*s; per 16-value group g (Q6_K) as
+ * d*sc_g*dx*sum((q6 - 32) * q).  out [nt][od] f32 is overwritten.
+ */
+int qmm_gemv(int qtype, const void *W, const int8_t *xq, const float *xds, float *out,
+             int64_t od, int64_t K, int64_t nt, void *stream);
+
+/*
+ * MMQ: matmul for any nt >= 1 on the tcgen05 tensor cores ([MMQ] sec. 2-6;
+ * [MOJO] "One mma per scale group").  Raw super-blocks are staged into
+ * shared memory by TMA, their nibbles (or 6-bit Q6_K codes minus 32) are
+ * unpacked in registers into exact small-integer f16 operands, one MMA chain
+ * per scale group accumulates the exact integer dot in TMEM (fp32, exact for
+ * these magnitudes), and the fp32 epilogue applies d, sc, dx, dmin, m and s.
+ * `workspace` (device, 16-byte aligned, >= qmm_gemm_workspace_bytes) holds
+ * an f16 copy of xq and the scale planes written by a prepass on `stream`;
+ * its contents need not be preserved between calls.  out is overwritten.
+ */
+int qmm_gemm(int qtype, const void *W, const int8_t *xq, const float *xds, float *out,
+             int64_t od, int64_t K, int64_t nt, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * The whole method from f32 activations: qmm_quantize_q8_1 into the caller's
+ * xq / xds buffers, then qmm_gemv (nt <= 8) or qmm_gemm (nt > 8), all on
+ * `stream` ([CH04] sec. 3.3: the GEMV / GEMM split by nt).  `workspace` may be
+ * NULL when qmm_matmul_workspace_bytes returns 0.
+ */
+int qmm_matmul(int qtype, const void *W, const float *x, int8_t *xq, float *xds, float *out,
+               int64_t od, int64_t K, int64_t nt, void *workspace, size_t ws_bytes,
+               void *stream);
+
+/*
+ * Test hook: the exact int32 block dots, computed by the same device dot code
+ * as a matmul path but written out before any scaling.
+ *   Q4_K: dots[t][r][j] = sum_{i<32} nibble[r][32j+i] * xq[t][32j+i], j < K/32
+ *   Q6_K: dots[t][r][g] = sum_{i<16} (q6[r][16g+i] - 32) * xq[t][16g+i], g < K/16
+ * path 0: the MMVQ (qmm_gemv) dot code, nt <= 8.
+ * path 1: the tensor-core (qmm_gemm) dot code; needs xds (for the prepass)
+ *         and a workspace of qmm_gemm_workspace_bytes.
+ * dots is a device buffer of nt*od*(K/32 or K/16) int32.
+ */
+int qmm_debug_block_dots(int qtype, const void *W, const int8_t *xq, const float *xds,
+                         int64_t od, int64_t K, int64_t nt, int32_t *dots, int path,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Synchronizes `stream`, then returns and clears the first error a kernel of
+ * this library recorded on the current device since the last call
+ * (QMM_ETIMEOUT when a bounded wait inside a kernel gave up), or QMM_ELAUNCH
+ * if the stream reports a CUDA error, else QMM_OK.
+ */
+int qmm_sync_status(void *stream);
+
+/* Test hook: when `on` is nonzero, the next tensor-core GEMM launches on the
+ * current device skip one producer arrival on purpose, so their bounded waits
+ * run out and report QMM_ETIMEOUT through qmm_sync_status (no trap, no hang:
+ * every wait gives up after about `ms` milliseconds).  Off by default. */
+int qmm_debug_inject_stall(int on, int ms);
+
+/* Static string for a status code. */
+const char *qmm_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

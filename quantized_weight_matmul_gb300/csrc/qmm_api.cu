@@ -1,0 +1,235 @@
+// qmm_api.cu -- the C ABI (include/qmm.h): host-side argument checks, the
+// nt-based choice between the MMVQ and the tensor-core path, and the device
+// status word bounded kernel waits report into.  Errors are returned, never
+// papered over by another path ("04 - Reading minfer's kernels II", sec. 3.3).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+
+#include "qmm_internal.h"
+
+namespace qmm {
+
+// First error recorded by a kernel on this device since the last
+// qmm_sync_status; 0 when none.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+std::atomic<int> g_stall_ms{0};
+
+bool valid_qtype(int q) { return q == QMM_Q4_K || q == QMM_Q6_K; }
+int block_bytes(int q) { return q == QMM_Q4_K ? 144 : (q == QMM_Q6_K ? 210 : 0); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int64_t od, int64_t K, int64_t nt) {
+  if (od < 1 || nt < 1 || K < 256 || K % 256) return QMM_EINVAL_SHAPE;
+  if (od > INT_MAX || K > INT_MAX || nt > INT_MAX) return QMM_EINVAL_SHAPE;
+  if (od * nt > INT_MAX || nt * K > INT_MAX || od * (K / 32) > INT_MAX) return QMM_EINVAL_SHAPE;
+  return QMM_OK;
+}
+
+// Device address of this device's status word (looked up once per device,
+// with that device current).
+int status_ptr(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMM_EDEVICE;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return QMM_EDEVICE;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return QMM_OK;
+}
+
+int check_device() {
+  static int cached[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMM_EDEVICE;
+  if (cached[dev] == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cached[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return cached[dev] == 1 ? QMM_OK : QMM_EDEVICE;
+}
+
+size_t gemm_ws(int64_t nt, int64_t K) { return gemm_xh_bytes(nt, K) + gemm_scl_bytes(nt, K); }
+
+int gemm_core(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
+              int64_t od, int64_t K, int64_t nt, void* ws, size_t ws_bytes, bool prep, cudaStream_t st) {
+  if (ws_bytes < gemm_ws(nt, K)) return QMM_EWORKSPACE;
+  if (!ws) return QMM_ENULL;
+  if (!aligned16(ws)) return QMM_EALIGN;
+  if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
+  int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  __half* xh = static_cast<__half*>(ws);
+  float* scl = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + gemm_xh_bytes(nt, K));
+  if (prep) {
+    rc = launch_gemm_prep(xq, xds, nt, K, gemm_ntp(nt), xh, scl, st);
+    if (rc) return rc;
+  }
+  return launch_gemm_tc(qtype, W, xh, scl, out, dots, od, K, nt, status, g_stall_ms.load(), st);
+}
+
+}  // namespace
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+size_t qmm_weight_bytes(int qtype, int64_t od, int64_t K) {
+  if (!valid_qtype(qtype) || od < 0 || K < 0 || K % 256) return 0;
+  return (size_t)od * (size_t)(K / 256) * (size_t)block_bytes(qtype);
+}
+
+size_t qmm_xq_bytes(int64_t nt, int64_t K) { return nt < 0 || K < 0 ? 0 : (size_t)nt * (size_t)K; }
+
+size_t qmm_xds_bytes(int64_t nt, int64_t K) {
+  return nt < 0 || K < 0 || K % 32 ? 0 : (size_t)nt * (size_t)(K / 32) * 2 * sizeof(float);
+}
+
+size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt) {
+  if (!valid_qtype(qtype) || check_shape(od, K, nt)) return 0;
+  return gemm_ws(nt, K);
+}
+
+size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt) {
+  if (!valid_qtype(qtype) || check_shape(od, K, nt)) return 0;
+  if (qtype == QMM_Q4_K && nt <= 8) return 0;
+  return gemm_ws(nt, K);
+}
+
+int qmm_gemv_max_nt(void) { return 8; }
+
+int qmm_quantize_q8_1(const float* x, int64_t nt, int64_t K, int8_t* xq, float* xds, void* stream) {
+  if (!x || !xq || !xds) return QMM_ENULL;
+  if (nt < 1 || K < 32 || K % 32 || nt > INT_MAX || K > INT_MAX || nt * K > INT_MAX) return QMM_EINVAL_SHAPE;
+  if (!aligned16(x) || !aligned16(xq) || !aligned16(xds)) return QMM_EALIGN;
+  int rc = check_device();
+  if (rc) return rc;
+  return launch_quantize(x, nt, K, xq, xds, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream));
+}
+
+int qmm_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int64_t od, int64_t K,
+             int64_t nt, void* stream) {
+  if (!valid_qtype(qtype)) return QMM_EINVAL_QTYPE;
+  if (qtype != QMM_Q4_K) return QMM_EINVAL_QTYPE;  // the MMVQ kernel covers Q4_K
+  if (!W || !xq || !xds || !out) return QMM_ENULL;
+  int rc = check_shape(od, K, nt);
+  if (rc) return rc;
+  if (nt > 8) return QMM_EINVAL_SHAPE;
+  if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
+  rc = check_device();
+  if (rc) return rc;
+  return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int qmm_gemm(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int64_t od, int64_t K,
+             int64_t nt, void* workspace, size_t ws_bytes, void* stream) {
+  if (!valid_qtype(qtype)) return QMM_EINVAL_QTYPE;
+  if (!W || !xq || !xds || !out) return QMM_ENULL;
+  int rc = check_shape(od, K, nt);
+  if (rc) return rc;
+  if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
+  rc = check_device();
+  if (rc) return rc;
+  return gemm_core(qtype, W, xq, xds, out, nullptr, od, K, nt, workspace, ws_bytes, true,
+                   static_cast<cudaStream_t>(stream));
+}
+
+int qmm_matmul(int qtype, const void* W, const float* x, int8_t* xq, float* xds, float* out, int64_t od,
+               int64_t K, int64_t nt, void* workspace, size_t ws_bytes, void* stream) {
+  if (!valid_qtype(qtype)) return QMM_EINVAL_QTYPE;
+  if (!W || !x || !xq || !xds || !out) return QMM_ENULL;
+  int rc = check_shape(od, K, nt);
+  if (rc) return rc;
+  if (!aligned16(W) || !aligned16(x) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
+  rc = check_device();
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (qtype == QMM_Q4_K && nt <= 8) {
+    rc = launch_quantize(x, nt, K, xq, xds, nullptr, nullptr, 0, st);
+    if (rc) return rc;
+    return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, nullptr, st);
+  }
+  if (ws_bytes < gemm_ws(nt, K)) return QMM_EWORKSPACE;
+  if (!workspace) return QMM_ENULL;
+  if (!aligned16(workspace)) return QMM_EALIGN;
+  if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
+  // the quantizer writes the tensor-core operands directly: no separate prepass
+  __half* xh = static_cast<__half*>(workspace);
+  float* scl = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gemm_xh_bytes(nt, K));
+  rc = launch_quantize(x, nt, K, xq, xds, xh, scl, gemm_ntp(nt), st);
+  if (rc) return rc;
+  return gemm_core(qtype, W, xq, xds, out, nullptr, od, K, nt, workspace, ws_bytes, false, st);
+}
+
+int qmm_debug_block_dots(int qtype, const void* W, const int8_t* xq, const float* xds, int64_t od, int64_t K,
+                         int64_t nt, int32_t* dots, int path, void* workspace, size_t ws_bytes, void* stream) {
+  if (!valid_qtype(qtype)) return QMM_EINVAL_QTYPE;
+  if (!W || !xq || !dots) return QMM_ENULL;
+  int rc = check_shape(od, K, nt);
+  if (rc) return rc;
+  if (!aligned16(W) || !aligned16(xq)) return QMM_EALIGN;
+  rc = check_device();
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (path == 0) {
+    if (qtype != QMM_Q4_K) return QMM_EINVAL_QTYPE;
+    if (nt > 8) return QMM_EINVAL_SHAPE;
+    return launch_gemv(qtype, W, xq, nullptr, nullptr, dots, od, K, nt, nullptr, st);
+  }
+  if (path != 1) return QMM_EINVAL_SHAPE;
+  if (!xds) return QMM_ENULL;
+  if (!aligned16(xds)) return QMM_EALIGN;
+  return gemm_core(qtype, W, xq, xds, nullptr, dots, od, K, nt, workspace, ws_bytes, true, st);
+}
+
+int qmm_sync_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QMM_ELAUNCH;
+  int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  int h = 0;
+  if (cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QMM_ELAUNCH;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return QMM_ELAUNCH;
+  }
+  return h;
+}
+
+int qmm_debug_inject_stall(int on, int ms) {
+  if (on && (ms < 1 || ms > 10000)) return QMM_EINVAL_SHAPE;
+  g_stall_ms.store(on ? ms : 0);
+  return QMM_OK;
+}
+
+const char* qmm_strerror(int status) {
+  switch (status) {
+    case QMM_OK: return "ok";
+    case QMM_EINVAL_QTYPE: return "unsupported weight type";
+    case QMM_EINVAL_SHAPE: return "invalid shape (od, K, nt)";
+    case QMM_EALIGN: return "pointer not 16-byte aligned";
+    case QMM_ENULL: return "required pointer is NULL";
+    case QMM_EWORKSPACE: return "workspace too small";
+    case QMM_ESMEM: return "shared memory request exceeds the device limit";
+    case QMM_ELAUNCH: return "CUDA launch or runtime error";
+    case QMM_ETIMEOUT: return "a bounded device-side wait timed out";
+    case QMM_EDEVICE: return "no usable sm_103 device is current";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// qmm_quantize.cu -- q8_1 activation quantizer and the tensor-core GEMM's
+// activation-operand prepass.
+//
+// q8_1 ("The quantized GEMM", mojo-dllm, section "The GPU path"): one warp per
+// 32-value block, one value per lane; the block maximum |x| and the integer
+// sum of the codes are warp-shuffle reductions; the scale d = amax/127 and the
+// code q = round-half-even(x/d) use IEEE f32 division; s = d * sum(q).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+namespace qmm {
+
+// One warp per 32-value block; grid-stride over all nt*K/32 blocks.
+// When xh / scl are non-null the same pass also writes the tensor-core GEMM
+// operands: the codes as exact f16 (xh [nt][K]) and the scales token-
+// contiguous (scl [K/32][ntp] float2 = (d, s)).
+__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restrict__ x, int64_t nblocks,
+                                                            int64_t nb_per_row, int8_t* __restrict__ xq,
+                                                            float2* __restrict__ xds,
+                                                            __half* __restrict__ xh,
+                                                            float2* __restrict__ scl, int64_t ntp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nblocks; b += warps) {
+    const float v = __ldg(x + b * 32 + lane);
+    float amax = fabsf(v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 127.0f);
+    int q = 0;
+    if (d != 0.0f) {
+      q = __float2int_rn(__fdiv_rn(v, d));
+      q = max(-127, min(127, q));
+    }
+    xq[b * 32 + lane] = (int8_t)q;
+    const int sum = __reduce_add_sync(0xffffffffu, q);
+    const float s = __fmul_rn(d, (float)sum);
+    if (xh) xh[b * 32 + lane] = __int2half_rn(q);
+    if (lane == 0) {
+      xds[b] = make_float2(d, s);
+      if (scl) {
+        const int64_t t = b / nb_per_row, j = b % nb_per_row;
+        scl[j * ntp + t] = make_float2(d, s);
+      }
+    }
+  }
+}
+
+// Prepass for qmm_gemm when the caller already holds xq / xds: 16 codes per
+// thread to f16, and the (d, s) pairs transposed to token-contiguous rows.
+__global__ void __launch_bounds__(256) gemm_operand_prep_kernel(const int8_t* __restrict__ xq,
+                                                                const float2* __restrict__ xds, int64_t nt,
+                                                                int64_t K, int64_t ntp,
+                                                                __half* __restrict__ xh,
+                                                                float2* __restrict__ scl) {
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t n16 = nt * K / 16;
+  for (int64_t i = tid; i < n16; i += stride) {
+    const int4 v = __ldg(reinterpret_cast<const int4*>(xq) + i);
+    const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 lo = __halves2half2(__int2half_rn((int8_t)(w[k] & 0xFF)),
+                                        __int2half_rn((int8_t)((w[k] >> 8) & 0xFF)));
+      const __half2 hi = __halves2half2(__int2half_rn((int8_t)((w[k] >> 16) & 0xFF)),
+                                        __int2half_rn((int8_t)((w[k] >> 24) & 0xFF)));
+      h[2 * k] = *reinterpret_cast<const uint32_t*>(&lo);
+      h[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+    }
+    int4* dst = reinterpret_cast<int4*>(xh) + 2 * i;
+    dst[0] = make_int4((int)h[0], (int)h[1], (int)h[2], (int)h[3]);
+    dst[1] = make_int4((int)h[4], (int)h[5], (int)h[6], (int)h[7]);
+  }
+  const int64_t nb = K / 32;
+  const int64_t nscl = nt * nb;
+  for (int64_t i = tid; i < nscl; i += stride) {
+    const int64_t t = i / nb, j = i % nb;
+    scl[j * ntp + t] = __ldg(xds + i);
+  }
+}
+
+static int grid_for(int64_t work_items, int per_block) {
+  int64_t g = (work_items + per_block - 1) / per_block;
+  const int64_t cap = 152LL * 16;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+int launch_quantize(const float* x, int64_t nt, int64_t K, int8_t* xq, float* xds, __half* xh,
+                    float* scl, int64_t ntp, cudaStream_t stream) {
+  const int64_t nblocks = nt * (K / 32);
+  if (nblocks == 0) return QMM_OK;
+  quantize_q8_1_kernel<<<grid_for(nblocks, 8), 256, 0, stream>>>(
+      x, nblocks, K / 32, xq, reinterpret_cast<float2*>(xds), xh, reinterpret_cast<float2*>(scl), ntp);
+  return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ELAUNCH;
+}
+
+int launch_gemm_prep(const int8_t* xq, const float* xds, int64_t nt, int64_t K, int64_t ntp, __half* xh,
+                     float* scl, cudaStream_t stream) {
+  const int64_t work = nt * K / 16;
+  gemm_operand_prep_kernel<<<grid_for(work, 256), 256, 0, stream>>>(
+      xq, reinterpret_cast<const float2*>(xds), nt, K, ntp, xh, reinterpret_cast<float2*>(scl));
+  return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ELAUNCH;
+}
+
+}  // namespace qmm

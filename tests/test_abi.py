@@ -1,0 +1,70 @@
+"""Host-side checks of the C ABI: the library loads, exports every function the
+header declares, and its size helpers / argument checks behave (no GPU work)."""
+import ctypes
+
+import pytest
+
+import quantized_weight_matmul_gb300 as qmm
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return qmm.load()
+
+
+def test_exports_every_header_function(lib):
+    names = qmm.header_functions()
+    assert len(names) >= 13
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # the Python binding carries the same names
+    assert all(hasattr(qmm, n) for n in names)
+
+
+def test_weight_and_activation_sizes():
+    assert qmm.qmm_weight_bytes(qmm.Q4_K, 4096, 4096) == 9437184
+    assert qmm.qmm_weight_bytes(qmm.Q4_K, 11008, 4096) == 25362432
+    assert qmm.qmm_weight_bytes(qmm.Q4_K, 14336, 4096) == 33030144
+    assert qmm.qmm_weight_bytes(qmm.Q6_K, 4096, 4096) == 13762560
+    assert qmm.qmm_weight_bytes(qmm.Q6_K, 32000, 4096) == 107520000
+    assert qmm.qmm_weight_bytes(qmm.Q4_K, 16, 300) == 0
+    assert qmm.qmm_weight_bytes(7, 16, 256) == 0
+    assert qmm.qmm_xq_bytes(3, 512) == 1536
+    assert qmm.qmm_xds_bytes(3, 512) == 3 * 16 * 8
+    assert qmm.qmm_gemv_max_nt() == 8
+    assert qmm.qmm_matmul_workspace_bytes(qmm.Q4_K, 4096, 4096, 8) == 0
+    ws = qmm.qmm_gemm_workspace_bytes(qmm.Q4_K, 4096, 4096, 512)
+    assert ws >= 512 * 4096 * 2 + 4096 // 32 * 512 * 8
+    assert qmm.qmm_matmul_workspace_bytes(qmm.Q4_K, 4096, 4096, 512) == ws
+    assert qmm.qmm_gemm_workspace_bytes(qmm.Q4_K, 4096, 4000, 512) == 0
+
+
+def test_argument_checks_need_no_device():
+    """Bad arguments are refused before any CUDA call."""
+    buf = ctypes.create_string_buffer(4096 + 16)
+    p = (ctypes.addressof(buf) + 15) & ~15
+    assert qmm.qmm_gemv(5, p, p, p, p, 256, 256, 1, 0) == qmm.QMM_EINVAL_QTYPE
+    assert qmm.qmm_gemv(qmm.Q4_K, 0, p, p, p, 256, 256, 1, 0) == qmm.QMM_ENULL
+    assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 300, 1, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 256, 9, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 0, 256, 1, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_gemv(qmm.Q4_K, p + 1, p, p, p, 256, 256, 1, 0) == qmm.QMM_EALIGN
+    assert qmm.qmm_quantize_q8_1(p, 1, 48, p, p, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_gemm(qmm.Q4_K, p, p, p, p, 256, 256, 0, p, 4096, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_debug_inject_stall(1, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_debug_inject_stall(0, 0) == qmm.QMM_OK
+
+
+def test_valid_call_without_a_gpu_fails_loudly():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    buf = ctypes.create_string_buffer(4096 + 16)
+    p = (ctypes.addressof(buf) + 15) & ~15
+    assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 256, 1, 0) == qmm.QMM_EDEVICE
+
+
+def test_strerror_covers_codes():
+    for code in range(0, -10, -1):
+        assert qmm.qmm_strerror(code) != "unknown status"
+    assert qmm.qmm_strerror(-99) == "unknown status"

@@ -1,0 +1,176 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+* q8_1 codes and scales: bit-exact.
+* int32 block dots (MMVQ and tensor-core dot code): bit-exact.
+* fp32 outputs: within 1e-4 of each output row's L2 norm (gpu_helpers).
+Shapes span several tiles with ragged tails, the edge cases (one row, one
+super-block, one token) and the five workload families at full size (the
+largest on a deterministic row sample).
+"""
+import numpy as np
+import pytest
+
+import quantized_weight_matmul_gb300 as qmm
+from gpu_helpers import assert_close_rows, dev, ora, oracle_rows, row_sample, threads
+from quantized_weight_matmul_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+Q4_K, Q6_K = qmm.Q4_K, qmm.Q6_K
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    qmm.load()
+
+
+def _case(qtype, od, K, nt, outliers=False, seed=0):
+    c = synth.Case(qtype, od, K, nt, outliers, seed)
+    return c.generate()
+
+
+# ------------------------------------------------------------- quantize ---
+
+@pytest.mark.parametrize("nt,K,outliers", [(1, 512, False), (8, 4096, True), (513, 4096, True),
+                                           (2048, 14336, False), (3, 96, False)])
+def test_quantize_bit_exact(nt, K, outliers):
+    x = synth.activations(nt, K, np.random.default_rng(nt + K), outliers)
+    if nt >= 3:
+        x[1, :64] = 0.0           # zero blocks
+        x[2, 32:64] = -1.25       # constant block
+        x[2, 0:32] = 0.0
+        x[2, 5] = 381.0           # d = 3 exactly
+        x[2, 6:10] = [1.5 * 3, 2.5 * 3, -0.5 * 3, 7.5 * 3]  # exact .5 quotients
+    xq, xds = qmm.quantize_q8_1(dev(x, torch))
+    oq, ods = ora().quantize_q8_1(x)
+    assert np.array_equal(xq.cpu().numpy(), oq)
+    assert np.array_equal(xds.cpu().numpy().view(np.uint32), ods.view(np.uint32))
+
+
+# ------------------------------------------------------------ block dots ---
+
+@pytest.mark.parametrize("od,K,nt", [(256, 512, 1), (256, 512, 8), (1000, 768, 3), (64, 14336, 2),
+                                     (4096, 4096, 1), (1, 256, 5)])
+def test_gemv_block_dots_bit_exact(od, K, nt):
+    W, x = _case(Q4_K, od, K, nt, seed=od)
+    xq, xds = ora().quantize_q8_1(x)
+    d = qmm.block_dots(Q4_K, dev(W, torch), dev(xq, torch), dev(xds, torch), od, path=0)
+    assert np.array_equal(d.cpu().numpy(), ora().block_dots(Q4_K, W, xq, od))
+
+
+@pytest.mark.parametrize("qtype,od,K,nt", [(Q4_K, 300, 512, 70), (Q4_K, 129, 1024, 200),
+                                           (Q4_K, 128, 256, 1), (Q6_K, 300, 2048, 70),
+                                           (Q6_K, 130, 4096, 131)])
+def test_gemm_block_dots_bit_exact(qtype, od, K, nt):
+    W, x = _case(qtype, od, K, nt, seed=od + nt)
+    xq, xds = ora().quantize_q8_1(x)
+    d = qmm.block_dots(qtype, dev(W, torch), dev(xq, torch), dev(xds, torch), od, path=1)
+    torch.cuda.synchronize()
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+    assert np.array_equal(d.cpu().numpy(), ora().block_dots(qtype, W, xq, od))
+
+
+# ---------------------------------------------------------------- GEMV ---
+
+@pytest.mark.parametrize("od,K,nt", [(256, 512, 1), (256, 512, 8), (1000, 768, 5), (1, 256, 2),
+                                     (4096, 4096, 1), (11008, 4096, 1), (14336, 4096, 2),
+                                     (14336, 4096, 4), (14336, 4096, 8), (4096, 14336, 2),
+                                     (4096, 14336, 4), (4096, 14336, 8)])
+def test_gemv_matches_oracle(od, K, nt):
+    W, x = _case(Q4_K, od, K, nt, outliers=(nt == 1), seed=0)
+    xq, xds = ora().quantize_q8_1(x)
+    out = qmm.gemv(Q4_K, dev(W, torch), dev(xq, torch), dev(xds, torch), od)
+    ref = ora().matmul_q8_1(Q4_K, W, xq, xds, od, nthreads=threads())
+    assert_close_rows(out.cpu().numpy(), ref, f"gemv {od}x{K} nt={nt}")
+
+
+# ---------------------------------------------------------------- GEMM ---
+
+@pytest.mark.parametrize("qtype,od,K,nt", [(Q4_K, 384, 1024, 9), (Q4_K, 384, 1024, 64),
+                                           (Q4_K, 384, 1024, 65), (Q4_K, 300, 1536, 130),
+                                           (Q4_K, 200, 512, 300), (Q4_K, 1, 256, 1),
+                                           (Q4_K, 1000, 768, 5), (Q6_K, 300, 2048, 33),
+                                           (Q6_K, 257, 4096, 200), (Q6_K, 64, 2048, 1)])
+def test_gemm_matches_oracle(qtype, od, K, nt):
+    W, x = _case(qtype, od, K, nt, outliers=True, seed=nt)
+    xq, xds = ora().quantize_q8_1(x)
+    out = qmm.gemm(qtype, dev(W, torch), dev(xq, torch), dev(xds, torch), od)
+    ref = ora().matmul_q8_1(qtype, W, xq, xds, od, nthreads=threads())
+    assert_close_rows(out.cpu().numpy(), ref, f"gemm q{qtype} {od}x{K} nt={nt}")
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+
+
+def _full_size(case):
+    W, x = case.generate()
+    Wd, xd = dev(W, torch), dev(x, torch)
+    out = qmm.matmul(case.qtype, Wd, xd, case.od).cpu().numpy()
+    rows = row_sample(case.od, max_rows=1024 if case.macs > 2e10 else 4096)
+    ref = oracle_rows(case.qtype, W, x, rows)
+    return assert_close_rows(out[:, rows], ref, case.name)
+
+
+@pytest.mark.parametrize("case", [c for w in ("tiny_q4k", "decode_gemv_q4k", "mmvq_q4k")
+                                  for c in synth.WORKLOADS[w].cases], ids=lambda c: c.name)
+def test_workload_small_batch(case):
+    _full_size(case)
+
+
+@pytest.mark.parametrize("case", synth.WORKLOADS["prefill_gemm_q4k"].cases, ids=lambda c: c.name)
+def test_workload_prefill(case):
+    _full_size(case)
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+
+
+@pytest.mark.parametrize("case", synth.WORKLOADS["skinny_q6k"].cases, ids=lambda c: c.name)
+def test_workload_skinny_q6k(case):
+    _full_size(case)
+
+
+def test_matmul_paths_agree_at_the_boundary():
+    """nt = 8 through MMVQ and through the tensor-core GEMM give the same result
+    to rounding."""
+    W, x = _case(Q4_K, 2048, 4096, 8, seed=3)
+    Wd, xd = dev(W, torch), dev(x, torch)
+    xq, xds = qmm.quantize_q8_1(xd)
+    a = qmm.gemv(Q4_K, Wd, xq, xds, 2048).cpu().numpy()
+    b = qmm.gemm(Q4_K, Wd, xq, xds, 2048).cpu().numpy()
+    assert_close_rows(a, b.astype(np.float64), "gemv vs gemm")
+
+
+# ------------------------------------------------------------- errors ---
+
+def test_errors_and_bounded_wait():
+    W, x = _case(Q4_K, 256, 512, 16, seed=1)
+    Wd, xd = dev(W, torch), dev(x, torch)
+    xq, xds = qmm.quantize_q8_1(xd)
+    out = torch.empty((16, 256), device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    # a workspace that is too small, a bad type, a misaligned pointer
+    ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    assert qmm.qmm_gemm(Q4_K, Wd.data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 16,
+                        ws.data_ptr(), 64, st) == qmm.QMM_EWORKSPACE
+    assert qmm.qmm_gemm(3, Wd.data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 16,
+                        ws.data_ptr(), 64, st) == qmm.QMM_EINVAL_QTYPE
+    assert qmm.qmm_gemv(Q4_K, Wd.data_ptr() + 8, xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 8,
+                        st) == qmm.QMM_EALIGN
+    # Q6_K needs a 16-byte row pitch for the tensor-core path (K % 2048 == 0)
+    assert qmm.qmm_gemm_workspace_bytes(Q6_K, 256, 512, 16) > 0
+    ws = qmm.workspace(qmm.qmm_gemm_workspace_bytes(Q6_K, 256, 512, 16), "cuda")
+    assert qmm.qmm_gemm(Q6_K, Wd.data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 16,
+                        ws.data_ptr(), ws.numel(), st) == qmm.QMM_EINVAL_SHAPE
+    # bounded wait: a skipped producer arrival makes the waits give up and report
+    assert qmm.qmm_sync_status(st) == qmm.QMM_OK
+    assert qmm.qmm_debug_inject_stall(1, 200) == qmm.QMM_OK
+    try:
+        qmm.gemm(Q4_K, Wd, xq, xds, 256)
+        assert qmm.qmm_sync_status(st) == qmm.QMM_ETIMEOUT
+    finally:
+        qmm.qmm_debug_inject_stall(0, 0)
+    # the context is still usable and the status word was cleared
+    ref = ora().matmul(Q4_K, W, x, 256)
+    got = qmm.gemm(Q4_K, Wd, xq, xds, 256).cpu().numpy()
+    assert qmm.qmm_sync_status(st) == qmm.QMM_OK
+    assert_close_rows(got, ref, "after timeout")
