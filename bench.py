@@ -273,7 +273,8 @@ def run_gpu(args):
     def step(copy, s=st):
         for i, c in enumerate(cases):
             rc = qmm.qmm_matmul(c.qtype, Wcopies[i][copy].data_ptr(), xs[i].data_ptr(), xqs[i].data_ptr(),
-                                xdss[i].data_ptr(), outs[i].data_ptr(), c.od, c.K, c.nt, 0, 0, s)
+                                xdss[i].data_ptr(), outs[i].data_ptr(), c.od, c.K, c.nt, 0, 0,
+                                qmm.QMM_FLAG_STATIC_WEIGHTS, s)
             if rc != qmm.QMM_OK:
                 raise qmm.QmmError(rc, "qmm_matmul")
 
@@ -314,22 +315,34 @@ def run_gpu(args):
     clocks = clk.summary()
     assert qmm.qmm_sync_status(st) == qmm.QMM_OK
 
-    # ---- roofline: the MMVQ kernel alone on the largest projection
+    # ---- roofline: the MMVQ kernel alone on the largest projection, launched
+    # back to back over the rotating copies from one CUDA graph (no host cost)
     big = max(range(len(cases)), key=lambda i: cases[i].weight_bytes)
     c = cases[big]
-    nrep = 64 * NCOPIES
+    nrep = 8 * NCOPIES
+
+    def gemv_run(k, s):
+        rc = qmm.qmm_gemv(c.qtype, Wcopies[big][k % NCOPIES].data_ptr(), xqs[big].data_ptr(),
+                          xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K, c.nt, s)
+        assert rc == qmm.QMM_OK
+
     with torch.cuda.stream(stream):
-        for k in range(NCOPIES):
-            qmm.qmm_gemv(c.qtype, Wcopies[big][k].data_ptr(), xqs[big].data_ptr(), xdss[big].data_ptr(),
-                         outs[big].data_ptr(), c.od, c.K, c.nt, st)
+        gemv_run(0, st)
+    stream.synchronize()
+    kg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(kg, stream=stream):
+        cs = torch.cuda.current_stream().cuda_stream
+        for k in range(nrep):
+            gemv_run(k, cs)
+    with torch.cuda.stream(stream):
+        kg.replay()
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         k0.record(stream)
-        for k in range(nrep):
-            qmm.qmm_gemv(c.qtype, Wcopies[big][k % NCOPIES].data_ptr(), xqs[big].data_ptr(),
-                         xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K, c.nt, st)
+        for _ in range(4):
+            kg.replay()
         k1.record(stream)
     torch.cuda.synchronize()
-    kernel_ms = k0.elapsed_time(k1) / nrep
+    kernel_ms = k0.elapsed_time(k1) / (4 * nrep)
     alg_bytes = c.weight_bytes + c.nt * c.K + c.nt * (c.K // 32) * 8 + c.nt * c.od * 4
     achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
     traffic = (NCU_TRAFFIC["bytes_per_launch"]
@@ -355,7 +368,7 @@ def run_gpu(args):
                 xs[i].copy_(xh[i], non_blocking=True)
                 rc = qmm.qmm_matmul(cc.qtype, Wcopies[i][s % NCOPIES].data_ptr(), xs[i].data_ptr(),
                                     xqs[i].data_ptr(), xdss[i].data_ptr(), outs[i].data_ptr(), cc.od, cc.K,
-                                    cc.nt, 0, 0, st)
+                                    cc.nt, 0, 0, qmm.QMM_FLAG_STATIC_WEIGHTS, st)
                 assert rc == qmm.QMM_OK
                 oh[i].copy_(outs[i], non_blocking=True)
         e1.record(stream)
@@ -410,8 +423,12 @@ def run_sweep(args):
     names = args.families.split(",") if args.families else list(synth.WORKLOADS)
     for fam in names:
         for c in synth.WORKLOADS[fam].cases:
+            if args.case and c.name != args.case:
+                continue
             W, x = c.generate()
             ncopy = max(2, min(32, int(4 * l2 // c.weight_bytes) + 1))
+            if args.copies:
+                ncopy = args.copies
             Ws = [torch.from_numpy(W).to(dev) for _ in range(ncopy)]
             xd = torch.from_numpy(x).to(dev)
             xq, xds = qmm.quantize_q8_1(xd)
@@ -421,22 +438,36 @@ def run_sweep(args):
             ws = qmm.workspace(need, dev)
             xh = ws.view(torch.uint8)
 
-            def launch(k):
+            def launch(k, s=st):
                 if use_gemv:
                     return qmm.qmm_gemv(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
-                                        c.od, c.K, c.nt, st)
+                                        c.od, c.K, c.nt, s)
                 return qmm.qmm_gemm(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
-                                    c.od, c.K, c.nt, xh.data_ptr(), need, st)
+                                    c.od, c.K, c.nt, xh.data_ptr(), need, s)
 
-            reps = max(ncopy, int(min(2000, 2e11 / max(c.macs, 1))))
+            reps = args.reps or max(ncopy, int(min(2000, 2e11 / max(c.macs, 1))))
             with torch.cuda.stream(stream):
                 for k in range(ncopy):
                     assert launch(k) == 0
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for k in range(reps):
-                    launch(k % ncopy)
-                e1.record(stream)
+            torch.cuda.synchronize()
+            if args.no_graph:
+                with torch.cuda.stream(stream):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for k in range(reps):
+                        launch(k % ncopy)
+                    e1.record(stream)
+            else:
+                gph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gph, stream=stream):
+                    st_cap = torch.cuda.current_stream().cuda_stream
+                    for k in range(reps):
+                        assert launch(k % ncopy, st_cap) == 0
+                with torch.cuda.stream(stream):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    gph.replay()
+                    e1.record(stream)
             torch.cuda.synchronize()
             assert qmm.qmm_sync_status(st) == 0
             us = e0.elapsed_time(e1) / reps * 1e3
@@ -461,6 +492,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--families", default="")
+    ap.add_argument("--case", default="", help="sweep: only the case with this name")
+    ap.add_argument("--reps", type=int, default=0, help="sweep: timed launches per case")
+    ap.add_argument("--copies", type=int, default=0, help="sweep: rotating weight copies per case")
+    ap.add_argument("--no-graph", action="store_true", help="sweep: launch from Python instead of a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -47,6 +47,9 @@
 extern "C" {
 #endif
 
+/* Flags of qmm_matmul. */
+#define QMM_FLAG_STATIC_WEIGHTS 1u /* see qmm_matmul */
+
 /* Weight block types.  12 is the GGML id of Q4_K ([MMQ] sec. 1); 14 is the
  * public GGML id of Q6_K. */
 typedef enum { QMM_Q4_K = 12, QMM_Q6_K = 14 } qmm_qtype;
@@ -78,7 +81,8 @@ size_t qmm_xds_bytes(int64_t nt, int64_t K);
  * token-contiguous scale planes, see qmm_gemm).  0 for invalid input. */
 size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
 
-/* Workspace qmm_matmul needs: qmm_gemm_workspace_bytes when nt > 8, else 0. */
+/* Workspace qmm_matmul needs: 0 on its MMVQ paths (Q4_K, nt <= 8), else
+ * qmm_gemm_workspace_bytes. */
 size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
 
 /* Largest nt qmm_gemv accepts (8, the register token loop of [MMQ] sec. 12). */
@@ -102,9 +106,11 @@ int qmm_quantize_q8_1(const float *x, int64_t nt, int64_t K, int8_t *xq, float *
  * MMVQ: small-batch matmul for 1 <= nt <= 8 ([CH04] sec. 3.4; [MMQ] sec. 12).
  * Streams every weight row once with 16-byte loads and keeps all nt tokens in
  * registers, so the weight traffic does not grow with nt.  Per 32-value
- * sub-block j (Q4_K) the integer dot D = sum(nibble * q) is rescaled as
- * d*sc_j*dx*D - dmin*m_j*s; per 16-value group g (Q6_K) as
- * d*sc_g*dx*sum((q6 - 32) * q).  out [nt][od] f32 is overwritten.
+ * sub-block j the integer dot D = sum(nibble * q) is rescaled as
+ * d*sc_j*dx*D - dmin*m_j*s.  Q4_K only (QMM_EINVAL_QTYPE for Q6_K, which
+ * qmm_matmul sends to the tensor-core path); QMM_ESMEM when the nt x K
+ * activations do not fit the kernel's shared memory next to its weight ring
+ * (nt*K*1.25 bytes above about 180 KB).  out [nt][od] f32 is overwritten.
  */
 int qmm_gemv(int qtype, const void *W, const int8_t *xq, const float *xds, float *out,
              int64_t od, int64_t K, int64_t nt, void *stream);
@@ -124,13 +130,24 @@ int qmm_gemm(int qtype, const void *W, const int8_t *xq, const float *xds, float
              int64_t od, int64_t K, int64_t nt, void *workspace, size_t ws_bytes, void *stream);
 
 /*
- * The whole method from f32 activations: qmm_quantize_q8_1 into the caller's
- * xq / xds buffers, then qmm_gemv (nt <= 8) or qmm_gemm (nt > 8), all on
- * `stream` ([CH04] sec. 3.3: the GEMV / GEMM split by nt).  `workspace` may be
- * NULL when qmm_matmul_workspace_bytes returns 0.
+ * The whole method from f32 activations, all on `stream` ([CH04] sec. 3.3:
+ * the small-batch / prefill split by nt):
+ *   - Q4_K with nt*K small enough (nt <= 4, nt*round_up(K, 2048) <= 16384,
+ *     the decode shapes): one fused kernel quantizes x to q8_1 inside the
+ *     MMVQ kernel (bit-identical codes) and writes xq / xds and out;
+ *   - other Q4_K with nt <= 8: qmm_quantize_q8_1 into xq / xds, then qmm_gemv;
+ *   - otherwise: qmm_quantize_q8_1 (which also writes the GEMM workspace),
+ *     then the tensor-core GEMM of qmm_gemm.
+ * The matmul kernels are launched as programmatic dependents of the kernel
+ * before them and wait for it before reading anything it may write.  With
+ * QMM_FLAG_STATIC_WEIGHTS the caller promises that W is not written by any
+ * work still in flight on `stream`; the weight stream then starts before the
+ * preceding kernel has completed (weights-once decode overlaps kernel
+ * boundaries).  `flags` = 0 is always safe.  `workspace` may be NULL when
+ * qmm_matmul_workspace_bytes returns 0.  Unknown flag bits: QMM_EINVAL_SHAPE.
  */
 int qmm_matmul(int qtype, const void *W, const float *x, int8_t *xq, float *xds, float *out,
-               int64_t od, int64_t K, int64_t nt, void *workspace, size_t ws_bytes,
+               int64_t od, int64_t K, int64_t nt, void *workspace, size_t ws_bytes, unsigned flags,
                void *stream);
 
 /*

@@ -38,6 +38,8 @@ QMM_ELAUNCH = -7
 QMM_ETIMEOUT = -8
 QMM_EDEVICE = -9
 
+QMM_FLAG_STATIC_WEIGHTS = 1
+
 _lock = threading.Lock()
 _lib = None
 
@@ -67,7 +69,8 @@ _SIGS = {
                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "qmm_matmul": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
-                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint,
+                                  ctypes.c_void_p]),
     "qmm_debug_block_dots": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                             ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
@@ -126,8 +129,8 @@ def qmm_gemv(qtype, W, xq, xds, out, od, K, nt, stream):
     return _call("qmm_gemv", qtype, W, xq, xds, out, od, K, nt, stream)
 def qmm_gemm(qtype, W, xq, xds, out, od, K, nt, workspace, ws_bytes, stream):
     return _call("qmm_gemm", qtype, W, xq, xds, out, od, K, nt, workspace, ws_bytes, stream)
-def qmm_matmul(qtype, W, x, xq, xds, out, od, K, nt, workspace, ws_bytes, stream):
-    return _call("qmm_matmul", qtype, W, x, xq, xds, out, od, K, nt, workspace, ws_bytes, stream)
+def qmm_matmul(qtype, W, x, xq, xds, out, od, K, nt, workspace, ws_bytes, flags, stream):
+    return _call("qmm_matmul", qtype, W, x, xq, xds, out, od, K, nt, workspace, ws_bytes, flags, stream)
 def qmm_debug_block_dots(qtype, W, xq, xds, od, K, nt, dots, path, workspace, ws_bytes, stream):
     return _call("qmm_debug_block_dots", qtype, W, xq, xds, od, K, nt, dots, path, workspace, ws_bytes, stream)
 def qmm_sync_status(stream): return _call("qmm_sync_status", stream)
@@ -193,7 +196,7 @@ def gemm(qtype, W, xq, xds, od, ws=None):
     return out
 
 
-def matmul(qtype, W, x, od, ws=None):
+def matmul(qtype, W, x, od, ws=None, flags=0, return_q8=False):
     """The whole method from f32 activations: quantize, then MMVQ or MMQ."""
     torch = _torch()
     nt, K = x.shape
@@ -204,8 +207,8 @@ def matmul(qtype, W, x, od, ws=None):
     if ws is None and need:
         ws = workspace(need, x.device)
     _check(qmm_matmul(qtype, _ptr(W), _ptr(x), _ptr(xq), _ptr(xds), _ptr(out), od, K, nt, _ptr(ws),
-                      0 if ws is None else ws.numel(), _stream()), "qmm_matmul")
-    return out
+                      0 if ws is None else ws.numel(), flags, _stream()), "qmm_matmul")
+    return (out, xq, xds) if return_q8 else out
 
 
 def block_dots(qtype, W, xq, xds, od, path):

@@ -105,7 +105,7 @@ size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt) {
 
 size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt) {
   if (!valid_qtype(qtype) || check_shape(od, K, nt)) return 0;
-  if (qtype == QMM_Q4_K && nt <= 8) return 0;
+  if (qtype == QMM_Q4_K && nt <= 8 && gemv_fits(nt, K)) return 0;
   return gemm_ws(nt, K);
 }
 
@@ -131,7 +131,11 @@ int qmm_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float
   if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
   rc = check_device();
   if (rc) return rc;
-  return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, nullptr, static_cast<cudaStream_t>(stream));
+  int* status = nullptr;
+  rc = status_ptr(&status);
+  if (rc) return rc;
+  return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, status, false,
+                     static_cast<cudaStream_t>(stream));
 }
 
 int qmm_gemm(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int64_t od, int64_t K,
@@ -148,7 +152,7 @@ int qmm_gemm(int qtype, const void* W, const int8_t* xq, const float* xds, float
 }
 
 int qmm_matmul(int qtype, const void* W, const float* x, int8_t* xq, float* xds, float* out, int64_t od,
-               int64_t K, int64_t nt, void* workspace, size_t ws_bytes, void* stream) {
+               int64_t K, int64_t nt, void* workspace, size_t ws_bytes, unsigned flags, void* stream) {
   if (!valid_qtype(qtype)) return QMM_EINVAL_QTYPE;
   if (!W || !x || !xq || !xds || !out) return QMM_ENULL;
   int rc = check_shape(od, K, nt);
@@ -156,11 +160,22 @@ int qmm_matmul(int qtype, const void* W, const float* x, int8_t* xq, float* xds,
   if (!aligned16(W) || !aligned16(x) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
   rc = check_device();
   if (rc) return rc;
+  if (flags & ~(unsigned)QMM_FLAG_STATIC_WEIGHTS) return QMM_EINVAL_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (qtype == QMM_Q4_K && nt <= 8) {
+  if (qtype == QMM_Q4_K && gemv_fused_fits(nt, K)) {
+    int* status = nullptr;
+    rc = status_ptr(&status);
+    if (rc) return rc;
+    return launch_gemv_fused(qtype, W, x, xq, xds, out, od, K, nt, status,
+                             (flags & QMM_FLAG_STATIC_WEIGHTS) != 0, st);
+  }
+  if (qtype == QMM_Q4_K && nt <= 8 && gemv_fits(nt, K)) {
+    int* status = nullptr;
+    rc = status_ptr(&status);
+    if (rc) return rc;
     rc = launch_quantize(x, nt, K, xq, xds, nullptr, nullptr, 0, st);
     if (rc) return rc;
-    return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, nullptr, st);
+    return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, status, true, st);
   }
   if (ws_bytes < gemm_ws(nt, K)) return QMM_EWORKSPACE;
   if (!workspace) return QMM_ENULL;
@@ -187,7 +202,11 @@ int qmm_debug_block_dots(int qtype, const void* W, const int8_t* xq, const float
   if (path == 0) {
     if (qtype != QMM_Q4_K) return QMM_EINVAL_QTYPE;
     if (nt > 8) return QMM_EINVAL_SHAPE;
-    return launch_gemv(qtype, W, xq, nullptr, nullptr, dots, od, K, nt, nullptr, st);
+    if (!xds) return QMM_ENULL;
+    int* status = nullptr;
+    rc = status_ptr(&status);
+    if (rc) return rc;
+    return launch_gemv(qtype, W, xq, xds, nullptr, dots, od, K, nt, status, false, st);
   }
   if (path != 1) return QMM_EINVAL_SHAPE;
   if (!xds) return QMM_ENULL;

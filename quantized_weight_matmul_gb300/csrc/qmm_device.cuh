@@ -74,6 +74,15 @@ __device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t 
   return d;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// Wait until the preceding grid in the stream has completed and its memory
+// is visible (a no-op when the kernel was not launched as a dependent).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid in the stream start its prologue.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ timing ----
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;

@@ -1,173 +1,507 @@
 // qmm_gemv.cu -- MMVQ: the small-batch (nt <= 8) Q4_K x q8_1 matmul.
 //
-// Design ("04 - Reading minfer's kernels II", sec. 3.4; "llama.cpp MMQ",
-// sec. 12.2): the weight matrix is streamed from HBM exactly once, with
-// 16-byte coalesced loads, and every weight block is dotted against all nt
-// tokens, whose accumulators live in registers -- the token count never
-// multiplies the weight traffic.  The dots are exact int32 (dp4a over
-// nibbles and int8 codes); the scales fold in once per 32-value sub-block:
-//     acc += d*sc_j*dx_j*D_j - dmin*m_j*s_j
-// ("The quantized GEMM", "The GPU path").
+// What it computes ("04 - Reading minfer's kernels II", sec. 3.4; "llama.cpp
+// MMQ", sec. 12.2; "The quantized GEMM", "The GPU path"): for every weight
+// row r and token t
+//     out[t][r] = sum_j ( d*sc_j*dx_tj*D_trj - dmin*m_j*s_tj ),
+//     D_trj = sum_{i<32} nibble[r][32j+i] * q[t][32j+i]   (exact int32, dp4a)
+// The weight matrix is streamed from HBM exactly once and every weight block
+// meets all nt tokens while it is on chip: nt never multiplies the weight
+// traffic.
 //
-// Mapping: one warp per weight row.  Lane l handles 16-byte chunk (l & 7) of
-// the 128 nibble bytes of super-block 4*i + (l >> 3) in iteration i, so one
-// warp instruction reads four consecutive super-blocks' nibbles (512 B) plus
-// their 16-byte headers (one broadcast load per 8 lanes).  Chunk c holds
-// bytes 16c..16c+15 of the nibble array: pair p = c/2, half h = c%2, i.e.
-// elements 64p+16h.. (low nibbles, sub-block 2p) and 64p+32+16h.. (high
-// nibbles, sub-block 2p+1).
+// GB300 design: a persistent grid, one CTA per SM, each CTA owning a
+// contiguous, balanced range of CR-row groups.  One producer thread keeps a
+// ring of shared-memory stages full with 2-D TMA tiles of the raw weight
+// bytes (CR rows x 8 super-blocks = 2048 k), so tens of KB per SM are in
+// flight whatever the consumers do.  Each consumer warp takes R rows of a
+// stage; lane l handles super-block l/4 of the stage and nibble pair p = l%4,
+// i.e. 64 consecutive weights (sub-blocks 2p and 2p+1), so its activation
+// slice is the same for all R rows.
+//
+// Two ways in for the activations:
+//   * staged: q8_1 codes and scales produced by the quantizer are copied
+//     once per CTA into shared memory (bulk copy);
+//   * fused: the consumer warps quantize the f32 activations themselves into
+//     shared memory (the same IEEE arithmetic as the quantizer, so the codes
+//     are bit-identical) and write the q8_1 outputs too -- one kernel per
+//     matmul instead of two, for the decode shapes where nt*K is small.
+// Kernels are launched as programmatic dependents of the preceding kernel
+// and let their own dependents start early, so consecutive matmuls overlap
+// their launch and ramp.  Every global access that may depend on the
+// preceding kernel waits for it (griddepcontrol.wait) -- except, when the
+// caller declares the weights static, the weight stream itself, which then
+// starts before the preceding kernel has finished.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
 
 namespace qmm {
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+namespace {
+
+constexpr int kSegSB = 8;                      // super-blocks per stage (2048 k)
+constexpr int kSegBytes = kSegSB * kQ4KBytes;  // 1152 B of one row per stage
+constexpr int kSmemBudget = 200 * 1024;        // staged path (large nt*K)
+constexpr int kFusedRing = 96 * 1024;          // fused path: two CTAs of consecutive kernels fit an SM
+constexpr int64_t kFusedMaxAct = 16384;        // fused path when nt*K <= this
+
+template <int NW, int R>
+struct GemvCfg {
+  static constexpr int CR = NW * R;  // rows per stage (R rows per consumer warp)
+  static constexpr int STAGE_BYTES = CR * kSegBytes;
+  static constexpr int THREADS = 32 * (NW + 1);
+};
+
+int64_t act_bytes_of(int64_t nt, int64_t K) { return nt * K + nt * (K / 32) * 8; }
+
+// The fused path pads each token's code plane to whole 2048-code stages.
+int64_t fused_plane(int64_t K) { return (K + 2047) / 2048 * 2048; }
+int64_t fused_act_bytes(int64_t nt, int64_t K) { return nt * fused_plane(K) + nt * (K / 32) * 8; }
+
+int stages_for(int64_t nt, int64_t K, int CR, int64_t budget) {
+  int s = (int)((budget - act_bytes_of(nt, K) - 1024 - 256) / ((int64_t)CR * kSegBytes));
+  return s > 8 ? 8 : s;
 }
 
-template <int NT, bool DOTS>
-__global__ void __launch_bounds__(256) gemv_q4k_kernel(const uint8_t* __restrict__ W,
-                                                       const int8_t* __restrict__ xq,
-                                                       const float* __restrict__ xds,
-                                                       float* __restrict__ out, int32_t* __restrict__ dots,
-                                                       int od, int K) {
-  constexpr int U = 4;  // iterations whose weight loads are issued together
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (row >= od) return;
-  const int lane = threadIdx.x & 31;
-  const int sbl = lane >> 3, c = lane & 7, p = c >> 1, h = c & 1;
-  const int nsb = K >> 8;
-  const int nb32 = K >> 5;
-  const uint8_t* wrow = W + (size_t)row * nsb * kQ4KBytes;
+// Decode the (scale, min) pairs of sub-blocks 2p and 2p+1 from the header
+// words holding scales[0..11] ("llama.cpp MMQ", sec. 6): sub-blocks 0-3 keep
+// both 6-bit codes in bytes j and j+4; sub-blocks 4-7 keep the low 4 bits in
+// the nibbles of byte j+4 and the top 2 bits in the top of bytes j-4 / j.
+// Returns the two codes of each kind in the low two bytes.
+__device__ __forceinline__ void q4k_pair_codes(uint32_t w1, uint32_t w2, uint32_t w3, int p, uint32_t& sc2,
+                                               uint32_t& m2) {
+  const uint32_t sh = 16u * (p & 1);
+  const uint32_t t1 = (w1 >> sh) & 0xFFFFu, t2 = (w2 >> sh) & 0xFFFFu, t3 = (w3 >> sh) & 0xFFFFu;
+  const uint32_t sc_low = t1 & 0x3F3Fu, m_low = t2 & 0x3F3Fu;
+  const uint32_t sc_high = (t3 & 0x0F0Fu) | ((t1 >> 2) & 0x3030u);
+  const uint32_t m_high = ((t3 >> 4) & 0x0F0Fu) | ((t2 >> 2) & 0x3030u);
+  sc2 = p < 2 ? sc_low : sc_high;
+  m2 = p < 2 ? m_low : m_high;
+}
 
-  float acc[NT];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+// Byte offset, in the fused path's shared activation plane of one token, of
+// code k: the 64 codes a lane reads per stage are split into four 16-byte
+// chunks stored chunk-major across the 32 lanes, so a warp's chunk loads
+// touch 32 consecutive 16-byte words (no bank conflicts).
+__device__ __forceinline__ int fused_code_offset(int k) {
+  const int seg = k >> 11, r = k & 2047;
+  return (((seg * 4 + ((r & 63) >> 4)) * 32 + (r >> 6)) << 4) + (r & 15);
+}
 
-  const int iters = (nsb + 3) >> 2;
-  for (int i0 = 0; i0 < iters; i0 += U) {
-    uint4 hdr[U], qs[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int sb = (i0 + u) * 4 + sbl;
-      if (i0 + u < iters && sb < nsb) {
-        const uint8_t* blk = wrow + (size_t)sb * kQ4KBytes;
-        hdr[u] = ldg_nc_v4(blk);
-        qs[u] = ldg_nc_v4(blk + 16 + 16 * c);
-      } else {
-        hdr[u] = make_uint4(0, 0, 0, 0);
-        qs[u] = make_uint4(0, 0, 0, 0);
-      }
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+template <int NT, int NW, int R, bool DOTS, bool FUSED>
+__global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
+    gemv_q4k_stream_kernel(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ x,
+                           int8_t* __restrict__ xq, float* __restrict__ xds, float* __restrict__ out,
+                           int32_t* __restrict__ dots, int od, int K, int stages, int* status, int static_w) {
+  using C = GemvCfg<NW, R>;
+  extern __shared__ uint8_t smem_dyn[];
+  const uint32_t s0 = smem_addr(smem_dyn);
+  const uint32_t pad = (1024u - (s0 & 1023u)) & 1023u;
+  uint8_t* smem = smem_dyn + pad;
+  const uint32_t sb = s0 + pad;
+
+  const int nsb = K >> 8, nseg = (nsb + kSegSB - 1) / kSegSB;
+  const int Kp = FUSED ? ((K + 2047) & ~2047) : K;  // per-token stride of the code plane
+  const int act_q = NT * Kp;                         // int8 codes
+  const int act_bytes = act_q + NT * (K >> 5) * 8;
+  const int act_off = stages * C::STAGE_BYTES;
+  const int bar_off = (act_off + act_bytes + 15) & ~15;
+  const uint32_t full0 = sb + bar_off, empty0 = full0 + 8 * stages, act_bar = empty0 + 8 * stages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + bar_off + 16 * stages + 8);
+  int8_t* sx = reinterpret_cast<int8_t*>(smem + act_off);
+  float* sds = reinterpret_cast<float*>(smem + act_off + act_q);
+
+  // CR-row groups of this CTA: a balanced split of all groups of the matrix
+  const int G = (od + C::CR - 1) / C::CR;
+  const int g_begin = (int)((int64_t)G * blockIdx.x / gridDim.x);
+  const int g_end = (int)((int64_t)G * (blockIdx.x + 1) / gridDim.x);
+  const int nchunks = (g_end - g_begin) * nseg;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Guard g{abort_flag, status, global_ns() + 4000ull * 1000000ull};
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, NW);
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int sb = (i0 + u) * 4 + sbl;
-      const bool live = (i0 + u < iters) && sb < nsb;
-      int sc_lo, m_lo, sc_hi, m_hi;
-      q4k_scale_min_words(hdr[u].y, hdr[u].z, hdr[u].w, 2 * p, sc_lo, m_lo);
-      q4k_scale_min_words(hdr[u].y, hdr[u].z, hdr[u].w, 2 * p + 1, sc_hi, m_hi);
-      const float d = half_bits_to_float(hdr[u].x);
-      const float dmin = half_bits_to_float(hdr[u].x >> 16);
-      const float a_lo = d * (float)sc_lo, a_hi = d * (float)sc_hi;
-      // the min term of a sub-block is added once, by the lane holding its first half
-      const float mm = h == 0 ? dmin : 0.0f;
-      const float c_lo = mm * (float)m_lo, c_hi = mm * (float)m_hi;
-      const uint32_t w[4] = {qs[u].x, qs[u].y, qs[u].z, qs[u].w};
-      uint32_t lo[4], hi[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        lo[k] = w[k] & 0x0F0F0F0Fu;
-        hi[k] = (w[k] >> 4) & 0x0F0F0F0Fu;
-      }
-      const int k_lo = sb * 256 + 64 * p + 16 * h;
-      const int j_lo = sb * 8 + 2 * p;
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        int dlo = 0, dhi = 0;
-        if (live) {
-          const int8_t* xt = xq + (size_t)t * K;
-          const int4 xl = __ldg(reinterpret_cast<const int4*>(xt + k_lo));
-          const int4 xh = __ldg(reinterpret_cast<const int4*>(xt + k_lo + 32));
-          dlo = __dp4a((int)lo[0], xl.x, dlo);
-          dlo = __dp4a((int)lo[1], xl.y, dlo);
-          dlo = __dp4a((int)lo[2], xl.z, dlo);
-          dlo = __dp4a((int)lo[3], xl.w, dlo);
-          dhi = __dp4a((int)hi[0], xh.x, dhi);
-          dhi = __dp4a((int)hi[1], xh.y, dhi);
-          dhi = __dp4a((int)hi[2], xh.z, dhi);
-          dhi = __dp4a((int)hi[3], xh.w, dhi);
+    mbar_init(act_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // the next kernel may launch now: it waits for this grid before touching
+  // anything this grid writes
+  griddep_launch_dependents();
+
+  if (warp == NW) {
+    // ----------------------------------------------------------- producer
+    if (lane == 0 && nchunks > 0) {
+      prefetch_tmap(&tmW);
+      if (!static_w) griddep_wait();
+      int issued = 0, st = 0, ph = 0, seg = 0, grp = g_begin;
+      bool act_issued = FUSED;
+      for (int c = 0; c < nchunks; ++c) {
+        if (c == stages && !act_issued) {
+          // the first stages of weights are in flight; now the activations,
+          // which the preceding kernel may still be writing
+          griddep_wait();
+          mbar_arrive_expect_tx(act_bar, (uint32_t)act_bytes);
+          bulk_load(sb + act_off, xq, (uint32_t)act_q, act_bar);
+          bulk_load(sb + act_off + act_q, xds, (uint32_t)(act_bytes - act_q), act_bar);
+          act_issued = true;
         }
-        if constexpr (DOTS) {
-          // the two halves of each sub-block sit in lanes c and c^1
-          const int flo = dlo + __shfl_xor_sync(0xffffffffu, dlo, 1);
-          const int fhi = dhi + __shfl_xor_sync(0xffffffffu, dhi, 1);
-          if (live && h == 0) {
-            int32_t* dst = dots + ((size_t)t * od + row) * nb32 + j_lo;
-            dst[0] = flo;
-            dst[1] = fhi;
+        if (!wait_bar(empty0 + 8 * st, ph ^ 1, g)) break;
+        mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE_BYTES);
+        tma_load_2d(sb + st * C::STAGE_BYTES, &tmW, seg * (kSegBytes / 8), grp * C::CR, full0 + 8 * st);
+        ++issued;
+        if (++st == stages) {
+          st = 0;
+          ph ^= 1;
+        }
+        if (++seg == nseg) {
+          seg = 0;
+          ++grp;
+        }
+      }
+      if (!act_issued) {
+        griddep_wait();
+        mbar_arrive_expect_tx(act_bar, (uint32_t)act_bytes);
+        bulk_load(sb + act_off, xq, (uint32_t)act_q, act_bar);
+        bulk_load(sb + act_off + act_q, xds, (uint32_t)(act_bytes - act_q), act_bar);
+      }
+      // drain: every copy in flight lands before the CTA exits
+      const uint64_t dl = global_ns() + 1000000000ull;
+      for (int i = issued - stages; i < issued; ++i) {
+        if (i < 0) continue;
+        for (uint32_t it = 0; !mbar_try_wait(full0 + 8 * (i % stages), (i / stages) & 1); ++it)
+          if ((it & 63u) == 63u && global_ns() > dl) break;
+      }
+      if (!FUSED)
+        for (uint32_t it = 0; !mbar_try_wait(act_bar, 0); ++it)
+          if ((it & 63u) == 63u && global_ns() > dl) break;
+    }
+  } else if (nchunks > 0) {
+    // ----------------------------------------------------------- consumers
+    const int sbo = lane >> 2, p = lane & 3;
+    bool ok = true;
+    griddep_wait();  // the preceding grid is complete before this thread reads x or writes
+    if (FUSED) {
+      // q8_1 of x [NT][K] into shared memory: eight lanes per 32-value block,
+      // four values per lane; block maximum and code sum by shuffles within
+      // the eight lanes; d = amax/127 and q = round-half-even(x/d) by IEEE
+      // division, s = d*(float)sum(q).  CTA (b mod grid) also writes block b
+      // of the xq / xds outputs.
+      const int nblk = NT * (K >> 5);
+      const int q8 = lane & 7;
+      for (int base = warp * 4; base < nblk; base += NW * 4) {
+        const int b = base + (lane >> 3);
+        const bool in = b < nblk;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (in) v = __ldg(reinterpret_cast<const float4*>(x + (size_t)b * 32 + q8 * 4));
+        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        const float d = __fdiv_rn(amax, 127.0f);
+        int q[4] = {0, 0, 0, 0};
+        if (d != 0.0f) {
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) q[i] = max(-127, min(127, __float2int_rn(__fdiv_rn(vv[i], d))));
+        }
+        int sum = q[0] + q[1] + q[2] + q[3];
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        const float s = __fmul_rn(d, (float)sum);
+        const uint32_t packed = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
+                                ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
+        if (in) {
+          const int t = b / (K >> 5), k = (b % (K >> 5)) * 32 + q8 * 4;
+          *reinterpret_cast<uint32_t*>(sx + t * Kp + fused_code_offset(k)) = packed;
+          if (q8 == 0) *reinterpret_cast<float2*>(sds + 2 * b) = make_float2(d, s);
+          if (b % gridDim.x == blockIdx.x) {
+            *reinterpret_cast<uint32_t*>(xq + (size_t)b * 32 + q8 * 4) = packed;
+            if (q8 == 0) reinterpret_cast<float2*>(xds)[b] = make_float2(d, s);
           }
-        } else if (live) {
-          const float4 sx = __ldg(reinterpret_cast<const float4*>(xds + ((size_t)t * nb32 + j_lo) * 2));
-          acc[t] = fmaf(a_lo * sx.x, (float)dlo, acc[t]);
-          acc[t] = fmaf(a_hi * sx.z, (float)dhi, acc[t]);
-          acc[t] = fmaf(-c_lo, sx.y, acc[t]);
-          acc[t] = fmaf(-c_hi, sx.w, acc[t]);
         }
+      }
+      named_barrier(1, 32 * NW);
+    } else {
+      ok = __all_sync(0xffffffffu, wait_bar(act_bar, 0, g));
+    }
+    float acc[R][NT];
+    int st = 0, ph = 0, seg = 0, grp = g_begin;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      if (seg == 0) {
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) acc[i][t] = 0.0f;
+      }
+      ok = __all_sync(0xffffffffu, wait_bar(full0 + 8 * st, ph, g));
+      if (!ok) break;
+      const int sbi = seg * kSegSB + sbo;  // super-block of this lane
+      const bool live = sbi < nsb;
+      const int kbase = sbi * 256 + 64 * p;
+      const int jlo = sbi * 8 + 2 * p;
+      const int row0 = grp * C::CR + warp * R;
+      // the R weight rows of this lane: nibbles split into the low (sub-block
+      // 2p) and high (sub-block 2p+1) planes, and the four scale factors
+      const uint8_t* stage = smem + st * C::STAGE_BYTES;
+      uint32_t lo[R][8], hi[R][8];
+      float a_lo[R], a_hi[R], c_lo[R], c_hi[R];
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const bool use = live && row0 + i < od;
+        uint4 hdr = make_uint4(0, 0, 0, 0), q0 = hdr, q1 = hdr;
+        if (use) {
+          const uint8_t* blk = stage + (warp * R + i) * kSegBytes + sbo * kQ4KBytes;
+          hdr = *reinterpret_cast<const uint4*>(blk);
+          q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * p);
+          q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * p);
+        }
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          lo[i][k] = w[k] & 0x0F0F0F0Fu;
+          hi[i][k] = (w[k] >> 4) & 0x0F0F0F0Fu;
+        }
+        uint32_t sc2, m2;
+        q4k_pair_codes(hdr.y, hdr.z, hdr.w, p, sc2, m2);
+        const float d = half_bits_to_float(hdr.x), dmin = half_bits_to_float(hdr.x >> 16);
+        a_lo[i] = d * (float)(sc2 & 0xFFu);
+        a_hi[i] = d * (float)(sc2 >> 8);
+        c_lo[i] = dmin * (float)(m2 & 0xFFu);
+        c_hi[i] = dmin * (float)(m2 >> 8);
+      }
+      if (live) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          // activation slice of token t: 64 codes and the two (d, s) pairs
+          uint4 x0, x1, x2, x3;
+          if (FUSED) {
+            const uint4* px = reinterpret_cast<const uint4*>(sx + t * Kp) + seg * 128 + lane;
+            x0 = px[0];
+            x1 = px[32];
+            x2 = px[64];
+            x3 = px[96];
+          } else {
+            const uint4* px = reinterpret_cast<const uint4*>(sx + t * K + kbase);
+            x0 = px[0];
+            x1 = px[1];
+            x2 = px[2];
+            x3 = px[3];
+          }
+          const float4 xs = *reinterpret_cast<const float4*>(sds + (t * (K >> 5) + jlo) * 2);
+          const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          const uint32_t yw[8] = {x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+          for (int i = 0; i < R; ++i) {
+            int dlo = 0, dhi = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              dlo = __dp4a((int)lo[i][k], (int)xw[k], dlo);
+              dhi = __dp4a((int)hi[i][k], (int)yw[k], dhi);
+            }
+            if constexpr (DOTS) {
+              if (row0 + i < od) {
+                int32_t* dst = dots + ((size_t)t * od + row0 + i) * (K >> 5) + jlo;
+                dst[0] = dlo;
+                dst[1] = dhi;
+              }
+            } else {
+              float a = acc[i][t];
+              a = fmaf(a_lo[i] * xs.x, (float)dlo, a);
+              a = fmaf(a_hi[i] * xs.z, (float)dhi, a);
+              a = fmaf(-c_lo[i], xs.y, a);
+              a = fmaf(-c_hi[i], xs.w, a);
+              acc[i][t] = a;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      if (!DOTS && seg == nseg - 1) {
+        // reduce the R x NT partial sums over the warp; lane i*NT+t stores (row i, token t)
+        float mine = 0.0f;
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            float v = acc[i][t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == i * NT + t) mine = v;
+          }
+        if (lane < R * NT) {
+          const int i = lane / NT, t = lane % NT;
+          if (row0 + i < od) out[(size_t)t * od + row0 + i] = mine;
+        }
+      }
+      if (++st == stages) {
+        st = 0;
+        ph ^= 1;
+      }
+      if (++seg == nseg) {
+        seg = 0;
+        ++grp;
       }
     }
   }
-  if constexpr (!DOTS) {
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      float v = acc[t];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      acc[t] = v;
-    }
-    if (lane < NT) {
-      float v = acc[0];
-#pragma unroll
-      for (int t = 1; t < NT; ++t)
-        if (lane == t) v = acc[t];
-      out[(size_t)lane * od + row] = v;
-    }
+  __syncthreads();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 gemv_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+struct GemvArgs {
+  const void* W;
+  const float* x;  // fused path
+  int8_t* xq;      // staged path: input; fused path: output
+  float* xds;      // likewise
+  float* out;
+  int32_t* dots;
+  int64_t od, K;
+  int* status;
+  bool pdl, static_w;
+  cudaStream_t stream;
+};
+
+template <int NT, int NW, int R, bool DOTS, bool FUSED>
+int launch_stream(const GemvArgs& a, int stages) {
+  using C = GemvCfg<NW, R>;
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QMM_EDEVICE;
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t act_bytes = FUSED ? fused_act_bytes(NT, a.K) : act_bytes_of(NT, a.K);
+  const int smem = stages * C::STAGE_BYTES + (int)((act_bytes + 15) & ~15) + 16 * stages + 32 + 1024;
+  auto kern = gemv_q4k_stream_kernel<NT, NW, R, DOTS, FUSED>;
+  static bool attr_done[64] = {};
+  if (dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 8192) !=
+        cudaSuccess)
+      return QMM_ESMEM;
+    attr_done[dev] = true;
   }
+  if (smem > kSmemBudget + 8192) return QMM_ESMEM;
+  auto fn = gemv_encode_fn();
+  if (!fn) return QMM_ELAUNCH;
+  // W viewed as [od][row_bytes/8] 8-byte elements; one box = CR rows x 8 super-blocks
+  const uint64_t row_bytes = (uint64_t)(a.K / 256) * kQ4KBytes;
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {row_bytes / 8, (cuuint64_t)a.od};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {kSegBytes / 8, (cuuint32_t)C::CR};
+  const cuuint32_t estr[2] = {1, 1};
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(a.W), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return QMM_ELAUNCH;
+  const int groups = (int)((a.od + C::CR - 1) / C::CR);
+  int grid = nsm > 0 ? nsm : 152;
+  if (grid > groups) grid = groups;
+  const int iod = (int)a.od, iK = (int)a.K, sw = a.static_w ? 1 : 0;
+  return launch_ex(kern, dim3(grid), dim3(C::THREADS), (size_t)smem, a.stream, a.pdl, m, a.x, a.xq, a.xds,
+                   a.out, a.dots, iod, iK, stages, a.status, sw);
+}
+
+// Staged path: consumer warps and rows per warp by nt -- 16 warps of one row
+// for nt <= 2, 16 warps of two rows for nt <= 4, 8 warps of four rows above
+// (the rows of a warp share its activation registers); fewer rows when the
+// activations leave too little shared memory for a 3-stage ring.  DOTS (a
+// test hook) uses 16 x 1.
+template <int NT, bool DOTS>
+int launch_staged(const GemvArgs& a) {
+  constexpr int NW = (DOTS || NT <= 4) ? 16 : 8;
+  constexpr int RP = DOTS ? 1 : (NT <= 2 ? 1 : (NT <= 4 ? 2 : 4));
+  int st = stages_for(NT, a.K, NW * RP, kSmemBudget);
+  if (st >= 3) return launch_stream<NT, NW, RP, DOTS, false>(a, st);
+  if constexpr (RP >= 2) {
+    st = stages_for(NT, a.K, NW * (RP / 2), kSmemBudget);
+    if (st >= 3) return launch_stream<NT, NW, RP / 2, DOTS, false>(a, st);
+  }
+  st = stages_for(NT, a.K, 8, kSmemBudget);
+  if (st >= 2) return launch_stream<NT, 8, 1, DOTS, false>(a, st);
+  return QMM_ESMEM;
+}
+
+// Fused path: 8 consumer warps of two rows (a 16-row, 18 KB stage) and a
+// ring of about 96 KB, so that a CTA of the next kernel fits on the SM next
+// to this one.
+template <int NT>
+int launch_fused(const GemvArgs& a) {
+  int st = (int)(kFusedRing / (16 * kSegBytes));
+  if (st > 8) st = 8;
+  if (st < 2) return QMM_ESMEM;
+  return launch_stream<NT, 8, 2, false, true>(a, st);
 }
 
 template <bool DOTS>
-static int launch_q4k(const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
-                      int64_t od, int64_t K, int64_t nt, cudaStream_t stream) {
-  const dim3 grid((unsigned)((od + 7) / 8)), block(256);
-  const uint8_t* w = static_cast<const uint8_t*>(W);
+int launch_q4k_staged(const GemvArgs& a, int64_t nt) {
   switch (nt) {
-#define QMM_GEMV_CASE(N) \
-  case N: gemv_q4k_kernel<N, DOTS><<<grid, block, 0, stream>>>(w, xq, xds, out, dots, (int)od, (int)K); break;
-    QMM_GEMV_CASE(1)
-    QMM_GEMV_CASE(2)
-    QMM_GEMV_CASE(3)
-    QMM_GEMV_CASE(4)
-    QMM_GEMV_CASE(5)
-    QMM_GEMV_CASE(6)
-    QMM_GEMV_CASE(7)
-    QMM_GEMV_CASE(8)
-#undef QMM_GEMV_CASE
+    case 1: return launch_staged<1, DOTS>(a);
+    case 2: return launch_staged<2, DOTS>(a);
+    case 3: return launch_staged<3, DOTS>(a);
+    case 4: return launch_staged<4, DOTS>(a);
+    case 5: return launch_staged<5, DOTS>(a);
+    case 6: return launch_staged<6, DOTS>(a);
+    case 7: return launch_staged<7, DOTS>(a);
+    case 8: return launch_staged<8, DOTS>(a);
     default: return QMM_EINVAL_SHAPE;
   }
-  return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ELAUNCH;
+}
+
+}  // namespace
+
+bool gemv_fits(int64_t nt, int64_t K) { return nt >= 1 && nt <= 8 && stages_for(nt, K, 8, kSmemBudget) >= 2; }
+
+bool gemv_fused_fits(int64_t nt, int64_t K) {
+  return nt >= 1 && nt <= 4 && nt * fused_plane(K) <= kFusedMaxAct;
 }
 
 int launch_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
-                int64_t od, int64_t K, int64_t nt, int* status, cudaStream_t stream) {
-  (void)status;
+                int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream) {
   if (qtype != QMM_Q4_K) return QMM_EINVAL_QTYPE;
-  return dots ? launch_q4k<true>(W, xq, xds, out, dots, od, K, nt, stream)
-              : launch_q4k<false>(W, xq, xds, out, dots, od, K, nt, stream);
+  if (!gemv_fits(nt, K)) return QMM_ESMEM;
+  // right after our quantizer the weight stream may start early: the quantizer
+  // releases its dependents only once everything before it has completed
+  const GemvArgs a{W,    nullptr, const_cast<int8_t*>(xq), const_cast<float*>(xds), out, dots, od, K, status,
+                   after_quantize, after_quantize, stream};
+  return dots ? launch_q4k_staged<true>(a, nt) : launch_q4k_staged<false>(a, nt);
+}
+
+int launch_gemv_fused(int qtype, const void* W, const float* x, int8_t* xq, float* xds, float* out, int64_t od,
+                      int64_t K, int64_t nt, int* status, bool static_w, cudaStream_t stream) {
+  if (qtype != QMM_Q4_K) return QMM_EINVAL_QTYPE;
+  if (!gemv_fused_fits(nt, K)) return QMM_ESMEM;
+  const GemvArgs a{W, x, xq, xds, out, nullptr, od, K, status, true, static_w, stream};
+  switch (nt) {
+    case 1: return launch_fused<1>(a);
+    case 2: return launch_fused<2>(a);
+    case 3: return launch_fused<3>(a);
+    case 4: return launch_fused<4>(a);
+    default: return QMM_EINVAL_SHAPE;
+  }
 }
 
 }  // namespace qmm

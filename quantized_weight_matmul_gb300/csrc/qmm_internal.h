@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -20,14 +21,47 @@ inline size_t gemm_xh_bytes(int64_t nt, int64_t K) {
 }
 inline size_t gemm_scl_bytes(int64_t nt, int64_t K) { return (size_t)(K / 32) * gemm_ntp(nt) * 8; }
 
+// Launch `kern` on `stream`; with `pdl` as a programmatic dependent of the
+// preceding kernel: it may start while that kernel drains and must call
+// griddepcontrol.wait before touching memory the preceding kernel writes.
+template <typename... KArgs, typename... Args>
+int launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) == cudaSuccess ? QMM_OK : QMM_ELAUNCH;
+}
+
 int launch_quantize(const float* x, int64_t nt, int64_t K, int8_t* xq, float* xds, __half* xh,
                     float* scl, int64_t ntp, cudaStream_t stream);
 int launch_gemm_prep(const int8_t* xq, const float* xds, int64_t nt, int64_t K, int64_t ntp, __half* xh,
                      float* scl, cudaStream_t stream);
 
-// MMVQ (nt <= 8).  dots != nullptr selects the raw block-dot output.
+// Whether the MMVQ kernel can stage nt x K activations next to its weight ring.
+bool gemv_fits(int64_t nt, int64_t K);
+// Whether the fused quantize + MMVQ kernel covers nt x K (decode shapes).
+bool gemv_fused_fits(int64_t nt, int64_t K);
+
+// MMVQ (nt <= 8).  dots != nullptr selects the raw block-dot output.  With
+// `after_quantize` the kernel is launched as a programmatic dependent of the
+// quantizer just enqueued (which releases it only once everything before it
+// is complete), so it may start streaming the weights before the activations
+// are ready.
 int launch_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
-                int64_t od, int64_t K, int64_t nt, int* status, cudaStream_t stream);
+                int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream);
+
+// Fused quantize + MMVQ: x f32 in, q8_1 (xq, xds) and out written.  With
+// `static_w` the weight stream starts before the preceding kernel completes.
+int launch_gemv_fused(int qtype, const void* W, const float* x, int8_t* xq, float* xds, float* out, int64_t od,
+                      int64_t K, int64_t nt, int* status, bool static_w, cudaStream_t stream);
 
 // Tensor-core GEMM over the prepared workspace.  dots != nullptr selects the
 // raw block-dot output (no scale folded into the weight operand).

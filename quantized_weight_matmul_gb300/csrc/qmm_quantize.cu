@@ -24,6 +24,11 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restr
                                                             float2* __restrict__ scl, int64_t ntp) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  // wait until the preceding grid is done (it may write x or read xq / xds),
+  // then let the next kernel -- the matmul -- start streaming its weights:
+  // everything enqueued before this grid is complete at that point
+  griddep_wait();
+  griddep_launch_dependents();
   for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nblocks; b += warps) {
     const float v = __ldg(x + b * 32 + lane);
     float amax = fabsf(v);
@@ -95,9 +100,9 @@ int launch_quantize(const float* x, int64_t nt, int64_t K, int8_t* xq, float* xd
                     float* scl, int64_t ntp, cudaStream_t stream) {
   const int64_t nblocks = nt * (K / 32);
   if (nblocks == 0) return QMM_OK;
-  quantize_q8_1_kernel<<<grid_for(nblocks, 8), 256, 0, stream>>>(
-      x, nblocks, K / 32, xq, reinterpret_cast<float2*>(xds), xh, reinterpret_cast<float2*>(scl), ntp);
-  return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ELAUNCH;
+  return launch_ex(quantize_q8_1_kernel, dim3(grid_for(nblocks, 8)), dim3(256), 0, stream, true, x, nblocks,
+                    (int64_t)(K / 32), xq, reinterpret_cast<float2*>(xds), xh, reinterpret_cast<float2*>(scl),
+                    ntp);
 }
 
 int launch_gemm_prep(const int8_t* xq, const float* xds, int64_t nt, int64_t K, int64_t ntp, __half* xh,

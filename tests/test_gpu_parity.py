@@ -129,6 +129,45 @@ def test_workload_skinny_q6k(case):
     _full_size(case)
 
 
+@pytest.mark.parametrize("od,K,nt,flags", [(4096, 4096, 1, 0), (4096, 4096, 1, 1), (1000, 512, 3, 1),
+                                           (300, 768, 4, 0), (11008, 4096, 2, 1), (64, 14336, 1, 1),
+                                           (129, 2304, 2, 0)])
+def test_fused_quantize_matmul(od, K, nt, flags):
+    """The fused quantize + MMVQ kernel (decode shapes): q8_1 outputs bit-exact,
+    matmul output within tolerance, with and without the static-weights flag."""
+    W, x = _case(Q4_K, od, K, nt, outliers=True, seed=od + K)
+    out, xq, xds = qmm.matmul(Q4_K, dev(W, torch), dev(x, torch), od, flags=flags, return_q8=True)
+    oq, ods = ora().quantize_q8_1(x)
+    assert np.array_equal(xq.cpu().numpy(), oq)
+    assert np.array_equal(xds.cpu().numpy().view(np.uint32), ods.view(np.uint32))
+    ref = ora().matmul_q8_1(Q4_K, W, oq, ods, od, nthreads=threads())
+    assert_close_rows(out.cpu().numpy(), ref, f"fused {od}x{K} nt={nt}")
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+
+
+def test_repeated_calls_are_bitwise_deterministic():
+    """Back-to-back calls on every path, interleaved with a large GEMM, give
+    bit-identical outputs (no stale or racing data between launches)."""
+    cases = [synth.Case(Q4_K, 4096, 4096, 1, True), synth.Case(Q4_K, 2048, 4096, 8),
+             synth.Case(Q6_K, 4096, 4096, 32), synth.Case(Q4_K, 1024, 4096, 96)]
+    big = synth.Case(Q4_K, 4096, 14336, 1024, True)
+    data = [(dev(W, torch), dev(x, torch)) for (W, x) in (c.generate() for c in cases)]
+    Wb, xb = (dev(a, torch) for a in big.generate())
+    first = [None] * len(cases)
+    for it in range(6):
+        if it % 2:
+            qmm.matmul(big.qtype, Wb, xb, big.od, flags=qmm.QMM_FLAG_STATIC_WEIGHTS)
+        for i, (c, (Wd, xd)) in enumerate(zip(cases, data)):
+            o = qmm.matmul(c.qtype, Wd, xd, c.od, flags=it % 2).cpu().numpy()
+            if first[i] is None:
+                first[i] = o
+            assert np.array_equal(o.view(np.uint32), first[i].view(np.uint32)), (c.name, it)
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+    for c, o in zip(cases, first):
+        W, x = c.generate()
+        assert_close_rows(o, ora().matmul(c.qtype, W, x, c.od, nthreads=threads()), c.name)
+
+
 def test_matmul_paths_agree_at_the_boundary():
     """nt = 8 through MMVQ and through the tensor-core GEMM give the same result
     to rounding."""
