@@ -20,13 +20,17 @@
 //               activation tile (BN x 64, 128-byte swizzle) and the
 //               token-contiguous (dx, s) rows of the same 64 k.
 //   warp 1      TMEM allocation and the single MMA-issuing thread: per scale
-//               group an MMA chain into one of two TMEM accumulators (ping-pong
-//               by group), committed to an mbarrier.
+//               group an MMA chain into one of four TMEM accumulators (round
+//               robin by group), committed to an mbarrier.
 //   warps 2-3   unpack: raw nibbles / 6-bit codes -> f16 operand tiles in the
 //               canonical no-swizzle K-major layout (Q4_K folds the 6-bit scale
 //               into the operand: sc*nibble is exact), one 64-k stage at a time.
 //   warps 4-11  epilogue: TMEM -> registers per group, fp32 rescale into
-//               register accumulators, one fp32 store at the end.
+//               register accumulators, one fp32 store at the end.  A TMEM
+//               accumulator is handed back to the MMA thread only after the
+//               epilogue has finished the arithmetic on the values it read
+//               from it; releasing it right after tcgen05.wait::ld produced
+//               rare wrong sums in stress runs, holding it does not.
 // Every wait is bounded: a wait that runs past its deadline raises the CTA's
 // abort flag and QMM_ETIMEOUT in the status word, all roles leave their
 // loops, in-flight copies and MMAs are drained, and TMEM is freed.
@@ -63,9 +67,9 @@ struct Cfg {
   static constexpr int SC_OFF = B_OFF + BS * B_BYTES;
   static constexpr int BAR_OFF = SC_OFF + BS * SC_BYTES;
   // barriers: raw full/empty, a full/empty, b full/empty, acc full/empty, done
-  static constexpr int NBARS = 2 * RS + 2 * AS + 2 * BS + 4 + 1;
+  static constexpr int NBARS = 2 * RS + 2 * AS + 2 * BS + 8 + 1;
   static constexpr int SMEM = BAR_OFF + NBARS * 8 + 16 + 1024;  // + slack for 1 KB alignment
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = 4 * BN;
   static_assert(RAW_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
   static_assert(SC_BYTES % 16 == 0, "align");
 };
@@ -80,8 +84,8 @@ struct Bars {
   __device__ uint32_t b_full(int i) const { return base + 8 * (2 * RS + 2 * AS + i); }
   __device__ uint32_t b_empty(int i) const { return base + 8 * (2 * RS + 2 * AS + BS + i); }
   __device__ uint32_t acc_full(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + i); }
-  __device__ uint32_t acc_empty(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 2 + i); }
-  __device__ uint32_t done() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 4); }
+  __device__ uint32_t acc_empty(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 4 + i); }
+  __device__ uint32_t done() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 8); }
 };
 
 // Wait used while draining: ignores the abort flag, gives up at `deadline`.
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bars.b_full(i), 1);
       mbar_init(bars.b_empty(i), 1 + 8);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(bars.acc_full(i), 1);
       mbar_init(bars.acc_empty(i), 8);
     }
@@ -313,8 +317,8 @@ __global__ void __launch_bounds__(384, 1)
         if (!wait_bar(bars.b_full(bs), (gs / C::BS) & 1, g)) break;
         tc_fence_after();
         for (int gi = 0; gi < C::GPS; ++gi, ++u) {
-          const int buf = u & 1;
-          if (!wait_bar(bars.acc_empty(buf), ((u >> 1) & 1) ^ 1, g)) {
+          const int buf = u & 3;
+          if (!wait_bar(bars.acc_empty(buf), ((u >> 2) & 1) ^ 1, g)) {
             ok = false;
             break;
           }
@@ -437,8 +441,8 @@ __global__ void __launch_bounds__(384, 1)
         const float* scp = reinterpret_cast<const float*>(smem + C::SC_OFF + bs * C::SC_BYTES);
 #pragma unroll
         for (int gi = 0; gi < C::GPS; ++gi, ++u) {
-          const int buf = u & 1;
-          if (!warp_wait(bars.acc_full(buf), (u >> 1) & 1, g)) {
+          const int buf = u & 3;
+          if (!warp_wait(bars.acc_full(buf), (u >> 2) & 1, g)) {
             ok = false;
             break;
           }
@@ -447,10 +451,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < CH; ++c)
             tc_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + hc * HALF + 32 * c), P[c]);
-          tc_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars.acc_empty(buf));
+#pragma unroll
+          for (int c = 0; c < CH; ++c) tc_wait_ld(P[c]);
           if (DOTS) {
             const int ng = QT == kQ4 ? (K >> 5) : (K >> 4);
             const int grp = QT == kQ4 ? 8 * b + 2 * s + gi : 16 * b + 4 * s + gi;
@@ -481,6 +483,10 @@ __global__ void __launch_bounds__(384, 1)
                 }
               }
           }
+          // hand the accumulator back only now, after its values were used
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.acc_empty(buf));
         }
         if (!ok) break;
         __syncwarp();

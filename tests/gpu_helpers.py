@@ -55,5 +55,11 @@ def assert_close_rows(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
     norm = np.linalg.norm(ref.astype(np.float64), axis=1)
     err = np.abs(gpu.astype(np.float64) - ref.astype(np.float64)).max(axis=1)
     rel = err / np.maximum(norm, 1e-30)
-    assert (rel <= REL_TOL).all(), f"{what}: worst row error {rel.max():.3e} of the row norm"
+    if not (rel <= REL_TOL).all():
+        full = np.abs(gpu.astype(np.float64) - ref.astype(np.float64)) / np.maximum(norm, 1e-30)[:, None]
+        bt, br = np.nonzero(full > REL_TOL)
+        raise AssertionError(
+            f"{what}: worst row error {rel.max():.3e} of the row norm; {len(bt)} outputs off, "
+            f"tokens {np.unique(bt)[:12].tolist()} ({len(np.unique(bt))}), columns {np.unique(br)[:12].tolist()} "
+            f"({len(np.unique(br))}), column tiles of 128: {np.unique(br // 128)[:12].tolist()}")
     return float(rel.max())

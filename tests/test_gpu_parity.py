@@ -168,6 +168,21 @@ def test_repeated_calls_are_bitwise_deterministic():
         assert_close_rows(o, ora().matmul(c.qtype, W, x, c.od, nthreads=threads()), c.name)
 
 
+@pytest.mark.parametrize("qtype,nt", [(Q6_K, 32), (Q6_K, 64), (Q4_K, 64), (Q4_K, 256)])
+def test_gemm_repeats_bitwise(qtype, nt):
+    """100 back-to-back tensor-core GEMMs of one problem are bit-identical: the
+    TMEM accumulators are never overwritten before the epilogue has used them
+    (an early hand-back showed up as rare wrong sums at 32- and 64-token
+    tiles)."""
+    c = synth.Case(qtype, 4096, 4096, nt)
+    Wd, xd = (dev(a, torch) for a in c.generate())
+    ws = qmm.workspace(qmm.qmm_matmul_workspace_bytes(qtype, c.od, c.K, nt), Wd.device)
+    first = qmm.matmul(qtype, Wd, xd, c.od, ws=ws)
+    bad = sum(int(not torch.equal(qmm.matmul(qtype, Wd, xd, c.od, ws=ws), first)) for _ in range(100))
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+    assert bad == 0, f"{bad} of 100 repeats differ"
+
+
 def test_matmul_paths_agree_at_the_boundary():
     """nt = 8 through MMVQ and through the tensor-core GEMM give the same result
     to rounding."""
