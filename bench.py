@@ -4,7 +4,8 @@
 Default workload (one "step"): the decode GEMV at nt = 1 on two Llama-7B-shaped
 Q4_K projections, od x K = 4096 x 4096 and 11008 x 4096, with x ~ N(0, 1) plus
 0.1% outliers x20.  A step runs the whole path for both: q8_1 quantization of
-x, then the MMVQ kernel (the nt <= 8 branch of the dispatch), through the C ABI.
+x and the MMVQ matmul (the decode branch of the dispatch, one fused kernel per
+projection), through the C ABI.
 
 value   weight GB/s of the whole job: weight bytes of all steps on all ranks /
         max-over-ranks wall time of the timed region, inputs resident in HBM.
@@ -14,15 +15,18 @@ value   weight GB/s of the whole job: weight bytes of all steps on all ranks /
 e2e     the same metric with the activations copied from pinned host memory and
         the outputs copied back inside every step, one qmm_matmul call per
         projection from Python.
-roofline  the MMVQ kernel alone on the 11008 x 4096 projection: algorithmic bytes
-        (weights + q8_1 activations + f32 outputs) per launch / its mean launch
-        time (CUDA events around back-to-back launches over rotating copies),
-        against the measured HBM copy bandwidth.
+roofline  the dominant kernel of the step -- the fused quantize + MMVQ kernel of
+        the 11008 x 4096 projection -- alone: algorithmic bytes (weights, f32
+        activations read, q8_1 activations and f32 outputs written) per launch
+        / its mean launch time (CUDA events around back-to-back launches over
+        rotating copies), against the measured HBM copy bandwidth.
 cpu_baseline  the CPU oracle (plain scalar C, all host cores) on the same step.
 
 --impl reference   times the CPU oracle alone as the reference arm.
---sweep            one JSON line per case of every workload family (kernel-only
-                   timings and roofline fractions); not the contract line.
+--sweep            one JSON line per case of every workload family: qmm_matmul
+                   (quantize + matmul from f32 activations; --kernel-only: the
+                   matmul kernel on q8_1 input) timings and roofline fractions;
+                   not the contract line.
 Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
 torch.distributed.run, one rank per GPU, each rank running the same workload on
 its own GPU (replicas; weak scaling).
@@ -47,10 +51,10 @@ METRIC = "Q4_K×q8_1 matmul TOPS & weight GB/s vs nt (1..512), % of HBM/int8 roo
 WORKLOAD = "decode_gemv_q4k"
 NCOPIES = 16
 
-# ncu capture of the MMVQ kernel (nt = 1, 11008 x 4096): dram read + write bytes
-# per launch, and the hash of qmm_gemv.cu it was taken on.  Reported as
-# roofline.traffic only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha1": None, "bytes_per_launch": None}
+# ncu capture of the fused quantize + MMVQ kernel (nt = 1, 11008 x 4096): dram
+# read + write bytes per launch, and the hash of qmm_gemv.cu it was taken on.
+# Reported as roofline.traffic only while the kernel source is unchanged.
+NCU_TRAFFIC = {"source_sha1": "e531fe7be29ac0183a01df2c6196bc153c60874e", "bytes_per_launch": 25402624}
 
 
 def log(*a):
@@ -268,7 +272,9 @@ def run_gpu(args):
     outs = [torch.empty((c.nt, c.od), dtype=torch.float32, device=dev) for c in cases]
     wbytes = sum(c.weight_bytes for c in cases)
     macs = sum(c.macs for c in cases)
-    launches_per_step = 2 * len(cases)  # quantize + MMVQ per projection
+    routes = [qmm.qmm_matmul_path(c.qtype, c.od, c.K, c.nt) for c in cases]
+    assert all(r > 0 for r in routes), routes
+    launches_per_step = sum(qmm.PATH_LAUNCHES[r] for r in routes)
 
     def step(copy, s=st):
         for i, c in enumerate(cases):
@@ -315,25 +321,32 @@ def run_gpu(args):
     clocks = clk.summary()
     assert qmm.qmm_sync_status(st) == qmm.QMM_OK
 
-    # ---- roofline: the MMVQ kernel alone on the largest projection, launched
-    # back to back over the rotating copies from one CUDA graph (no host cost)
+    # ---- roofline: the dominant kernel of the step -- the matmul kernel of the
+    # largest projection -- launched back to back over the rotating copies
+    # from one CUDA graph (no host cost), exactly as the step launches it
     big = max(range(len(cases)), key=lambda i: cases[i].weight_bytes)
     c = cases[big]
+    route = routes[big]
     nrep = 8 * NCOPIES
 
-    def gemv_run(k, s):
-        rc = qmm.qmm_gemv(c.qtype, Wcopies[big][k % NCOPIES].data_ptr(), xqs[big].data_ptr(),
-                          xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K, c.nt, s)
+    def kern_run(k, s):
+        if route == qmm.QMM_PATH_FUSED_MMVQ:
+            rc = qmm.qmm_matmul(c.qtype, Wcopies[big][k % NCOPIES].data_ptr(), xs[big].data_ptr(),
+                                xqs[big].data_ptr(), xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K,
+                                c.nt, 0, 0, qmm.QMM_FLAG_STATIC_WEIGHTS, s)
+        else:
+            rc = qmm.qmm_gemv(c.qtype, Wcopies[big][k % NCOPIES].data_ptr(), xqs[big].data_ptr(),
+                              xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K, c.nt, s)
         assert rc == qmm.QMM_OK
 
     with torch.cuda.stream(stream):
-        gemv_run(0, st)
+        kern_run(0, st)
     stream.synchronize()
     kg = torch.cuda.CUDAGraph()
     with torch.cuda.graph(kg, stream=stream):
         cs = torch.cuda.current_stream().cuda_stream
         for k in range(nrep):
-            gemv_run(k, cs)
+            kern_run(k, cs)
     with torch.cuda.stream(stream):
         kg.replay()
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -343,14 +356,21 @@ def run_gpu(args):
         k1.record(stream)
     torch.cuda.synchronize()
     kernel_ms = k0.elapsed_time(k1) / (4 * nrep)
-    alg_bytes = c.weight_bytes + c.nt * c.K + c.nt * (c.K // 32) * 8 + c.nt * c.od * 4
+    act_q8 = c.nt * c.K + c.nt * (c.K // 32) * 8  # q8_1 codes + (d, s)
+    if route == qmm.QMM_PATH_FUSED_MMVQ:
+        # weights + f32 x read + q8_1 written + f32 out written
+        alg_bytes = c.weight_bytes + c.nt * c.K * 4 + act_q8 + c.nt * c.od * 4
+        kname = "gemv_q4k_stream_kernel<nt=1, fused> (quantize + MMVQ)"
+    else:
+        alg_bytes = c.weight_bytes + act_q8 + c.nt * c.od * 4
+        kname = "gemv_q4k_stream_kernel (MMVQ)"
     achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
     traffic = (NCU_TRAFFIC["bytes_per_launch"]
                if NCU_TRAFFIC["source_sha1"] == source_sha1("quantized_weight_matmul_gb300/csrc/qmm_gemv.cu")
                else None)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": "gemv_q4k_kernel<1> (MMVQ)", "shape": [c.od, c.K], "kernel_us": kernel_ms * 1e3,
+                "kernel": kname, "shape": [c.od, c.K], "kernel_us": kernel_ms * 1e3,
                 "alg_bytes_per_launch": alg_bytes, "peak_source": peaks["source"] + " hbm_gbs (copy)"}
 
     # ---- e2e: host activations in, host outputs back, one C-ABI call per projection
@@ -410,7 +430,8 @@ def run_gpu(args):
 
 
 def run_sweep(args):
-    """Kernel-only timing of every case of every workload family."""
+    """Timing of every case of every workload family (CUDA graph of back-to-back
+    calls over rotating weight copies)."""
     import torch
     import quantized_weight_matmul_gb300 as qmm
     from quantized_weight_matmul_gb300 import synth
@@ -433,17 +454,23 @@ def run_sweep(args):
             xd = torch.from_numpy(x).to(dev)
             xq, xds = qmm.quantize_q8_1(xd)
             out = torch.empty((c.nt, c.od), dtype=torch.float32, device=dev)
-            use_gemv = c.qtype == qmm.Q4_K and c.nt <= 8
+            route = qmm.qmm_matmul_path(c.qtype, c.od, c.K, c.nt)
+            use_gemv = c.qtype == qmm.Q4_K and c.nt <= 8 and route != qmm.QMM_PATH_MMQ
             need = qmm.qmm_gemm_workspace_bytes(c.qtype, c.od, c.K, c.nt)
             ws = qmm.workspace(need, dev)
-            xh = ws.view(torch.uint8)
+            xq8 = torch.empty((c.nt, c.K), dtype=torch.int8, device=dev)
+            xds8 = torch.empty((c.nt, c.K // 32, 2), dtype=torch.float32, device=dev)
 
             def launch(k, s=st):
+                if not args.kernel_only:  # the whole path from f32 activations
+                    return qmm.qmm_matmul(c.qtype, Ws[k].data_ptr(), xd.data_ptr(), xq8.data_ptr(),
+                                          xds8.data_ptr(), out.data_ptr(), c.od, c.K, c.nt, ws.data_ptr(), need,
+                                          qmm.QMM_FLAG_STATIC_WEIGHTS, s)
                 if use_gemv:
                     return qmm.qmm_gemv(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
                                         c.od, c.K, c.nt, s)
                 return qmm.qmm_gemm(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
-                                    c.od, c.K, c.nt, xh.data_ptr(), need, s)
+                                    c.od, c.K, c.nt, ws.data_ptr(), need, s)
 
             reps = args.reps or max(ncopy, int(min(2000, 2e11 / max(c.macs, 1))))
             with torch.cuda.stream(stream):
@@ -471,13 +498,17 @@ def run_sweep(args):
             torch.cuda.synchronize()
             assert qmm.qmm_sync_status(st) == 0
             us = e0.elapsed_time(e1) / reps * 1e3
-            alg = c.weight_bytes + c.nt * c.K * 1.25 + c.nt * c.od * 4
+            # weights + q8_1 activations (+ the f32 activations they come from) + f32 out
+            alg = c.weight_bytes + c.nt * c.K * 1.25 + c.nt * c.od * 4 + (0 if args.kernel_only else c.nt * c.K * 4)
             tops = 2 * c.macs / (us / 1e6) / 1e12
-            rec = {"case": c.name, "path": "mmvq" if use_gemv else "mmq-tcgen05", "us": us,
+            names = {qmm.QMM_PATH_FUSED_MMVQ: "fused quantize+mmvq", qmm.QMM_PATH_MMVQ: "quantize, mmvq",
+                     qmm.QMM_PATH_MMQ: "quantize, mmq-tcgen05"}
+            what = (("mmvq" if use_gemv else "mmq-tcgen05 (with its operand prepass)") if args.kernel_only
+                    else names[route])
+            rec = {"case": c.name, "path": what, "us": us,
                    "weight_GBs": c.weight_bytes / (us / 1e6) / 1e9, "TOPS": tops,
                    "hbm_frac": alg / (us / 1e6) / 1e9 / peaks["hbm_gbs"],
-                   "tensor_frac_f16": tops / peaks["bf16_tflops"], "copies": ncopy, "reps": reps,
-                   "note": "gemm time includes its activation prepass" if not use_gemv else ""}
+                   "tensor_frac_f16": tops / peaks["bf16_tflops"], "copies": ncopy, "reps": reps}
             print(json.dumps(rec), flush=True)
             del Ws, ws
             torch.cuda.empty_cache()
@@ -496,6 +527,8 @@ def main():
     ap.add_argument("--reps", type=int, default=0, help="sweep: timed launches per case")
     ap.add_argument("--copies", type=int, default=0, help="sweep: rotating weight copies per case")
     ap.add_argument("--no-graph", action="store_true", help="sweep: launch from Python instead of a CUDA graph")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="sweep: time qmm_gemv / qmm_gemm on pre-quantized activations instead of qmm_matmul")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -85,6 +85,16 @@ size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
  * qmm_gemm_workspace_bytes. */
 size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
 
+/* Routes of qmm_matmul (see there), as returned by qmm_matmul_path. */
+#define QMM_PATH_FUSED_MMVQ 1 /* one kernel: quantize inside the MMVQ kernel  */
+#define QMM_PATH_MMVQ 2       /* two kernels: quantizer, then MMVQ            */
+#define QMM_PATH_MMQ 3        /* two kernels: quantizer, then tensor-core GEMM */
+
+/* The route qmm_matmul takes for this problem (a QMM_PATH_* value), or the
+ * negative QMM_E* code qmm_matmul would return for the shape or type.  Host
+ * only; it depends on nothing but its arguments. */
+int qmm_matmul_path(int qtype, int64_t od, int64_t K, int64_t nt);
+
 /* Largest nt qmm_gemv accepts (8, the register token loop of [MMQ] sec. 12). */
 int qmm_gemv_max_nt(void);
 

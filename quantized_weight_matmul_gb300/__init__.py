@@ -40,6 +40,12 @@ QMM_EDEVICE = -9
 
 QMM_FLAG_STATIC_WEIGHTS = 1
 
+QMM_PATH_FUSED_MMVQ = 1
+QMM_PATH_MMVQ = 2
+QMM_PATH_MMQ = 3
+# kernels one qmm_matmul call launches on each route
+PATH_LAUNCHES = {QMM_PATH_FUSED_MMVQ: 1, QMM_PATH_MMVQ: 2, QMM_PATH_MMQ: 2}
+
 _lock = threading.Lock()
 _lib = None
 
@@ -58,6 +64,7 @@ _SIGS = {
                                                    ctypes.c_int64]),
     "qmm_matmul_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                                      ctypes.c_int64]),
+    "qmm_matmul_path": (ctypes.c_int, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
     "qmm_gemv_max_nt": (ctypes.c_int, []),
     "qmm_quantize_q8_1": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_void_p]),
@@ -123,6 +130,7 @@ def qmm_xq_bytes(nt, K): return _call("qmm_xq_bytes", nt, K)
 def qmm_xds_bytes(nt, K): return _call("qmm_xds_bytes", nt, K)
 def qmm_gemm_workspace_bytes(qtype, od, K, nt): return _call("qmm_gemm_workspace_bytes", qtype, od, K, nt)
 def qmm_matmul_workspace_bytes(qtype, od, K, nt): return _call("qmm_matmul_workspace_bytes", qtype, od, K, nt)
+def qmm_matmul_path(qtype, od, K, nt): return _call("qmm_matmul_path", qtype, od, K, nt)
 def qmm_gemv_max_nt(): return _call("qmm_gemv_max_nt")
 def qmm_quantize_q8_1(x, nt, K, xq, xds, stream): return _call("qmm_quantize_q8_1", x, nt, K, xq, xds, stream)
 def qmm_gemv(qtype, W, xq, xds, out, od, K, nt, stream):

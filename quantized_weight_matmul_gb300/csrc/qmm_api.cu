@@ -62,6 +62,14 @@ int check_device() {
 
 size_t gemm_ws(int64_t nt, int64_t K) { return gemm_xh_bytes(nt, K) + gemm_scl_bytes(nt, K); }
 
+// The qmm_matmul route for a valid problem (one place, so the query below and
+// the dispatch cannot disagree).
+int matmul_route(int qtype, int64_t nt, int64_t K) {
+  if (qtype == QMM_Q4_K && gemv_fused_fits(nt, K)) return QMM_PATH_FUSED_MMVQ;
+  if (qtype == QMM_Q4_K && nt <= 8 && gemv_fits(nt, K)) return QMM_PATH_MMVQ;
+  return QMM_PATH_MMQ;
+}
+
 int gemm_core(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
               int64_t od, int64_t K, int64_t nt, void* ws, size_t ws_bytes, bool prep, cudaStream_t st) {
   if (ws_bytes < gemm_ws(nt, K)) return QMM_EWORKSPACE;
@@ -105,8 +113,17 @@ size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt) {
 
 size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt) {
   if (!valid_qtype(qtype) || check_shape(od, K, nt)) return 0;
-  if (qtype == QMM_Q4_K && nt <= 8 && gemv_fits(nt, K)) return 0;
+  if (matmul_route(qtype, nt, K) != QMM_PATH_MMQ) return 0;
   return gemm_ws(nt, K);
+}
+
+int qmm_matmul_path(int qtype, int64_t od, int64_t K, int64_t nt) {
+  if (!valid_qtype(qtype)) return QMM_EINVAL_QTYPE;
+  int rc = check_shape(od, K, nt);
+  if (rc) return rc;
+  const int path = matmul_route(qtype, nt, K);
+  if (path == QMM_PATH_MMQ && qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
+  return path;
 }
 
 int qmm_gemv_max_nt(void) { return 8; }
@@ -162,14 +179,15 @@ int qmm_matmul(int qtype, const void* W, const float* x, int8_t* xq, float* xds,
   if (rc) return rc;
   if (flags & ~(unsigned)QMM_FLAG_STATIC_WEIGHTS) return QMM_EINVAL_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (qtype == QMM_Q4_K && gemv_fused_fits(nt, K)) {
+  const int path = matmul_route(qtype, nt, K);
+  if (path == QMM_PATH_FUSED_MMVQ) {
     int* status = nullptr;
     rc = status_ptr(&status);
     if (rc) return rc;
     return launch_gemv_fused(qtype, W, x, xq, xds, out, od, K, nt, status,
                              (flags & QMM_FLAG_STATIC_WEIGHTS) != 0, st);
   }
-  if (qtype == QMM_Q4_K && nt <= 8 && gemv_fits(nt, K)) {
+  if (path == QMM_PATH_MMVQ) {
     int* status = nullptr;
     rc = status_ptr(&status);
     if (rc) return rc;

@@ -68,3 +68,23 @@ def test_strerror_covers_codes():
     for code in range(0, -10, -1):
         assert qmm.qmm_strerror(code) != "unknown status"
     assert qmm.qmm_strerror(-99) == "unknown status"
+
+
+def test_matmul_route_query():
+    """qmm_matmul_path names the route the dispatch takes: the fused decode
+    kernel for small nt*K, quantize + MMVQ up to nt = 8, the tensor-core GEMM
+    beyond (and for Q6_K); workspace is needed exactly on the GEMM route."""
+    Q4, Q6 = qmm.Q4_K, qmm.Q6_K
+    cases = [((Q4, 4096, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 11008, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ),
+             ((Q4, 256, 512, 4), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 4096, 4096, 4), qmm.QMM_PATH_FUSED_MMVQ),
+             ((Q4, 4096, 4096, 5), qmm.QMM_PATH_MMVQ), ((Q4, 4096, 4096, 8), qmm.QMM_PATH_MMVQ),
+             ((Q4, 4096, 14336, 2), qmm.QMM_PATH_MMVQ), ((Q4, 4096, 4096, 9), qmm.QMM_PATH_MMQ),
+             ((Q4, 4096, 4096, 512), qmm.QMM_PATH_MMQ), ((Q6, 4096, 4096, 1), qmm.QMM_PATH_MMQ),
+             ((Q6, 32000, 4096, 80), qmm.QMM_PATH_MMQ)]
+    for args, path in cases:
+        assert qmm.qmm_matmul_path(*args) == path, args
+        assert (qmm.qmm_matmul_workspace_bytes(*args) > 0) == (path == qmm.QMM_PATH_MMQ), args
+    assert qmm.qmm_matmul_path(Q6, 4096, 768, 32) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_matmul_path(Q4, 4096, 300, 1) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_matmul_path(Q4, 4096, 4096, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_matmul_path(3, 4096, 4096, 1) == qmm.QMM_EINVAL_QTYPE
