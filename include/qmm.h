@@ -140,6 +140,37 @@ int qmm_gemm(int qtype, const void *W, const int8_t *xq, const float *xds, float
              int64_t od, int64_t K, int64_t nt, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * qmm_gemm for callers that cannot allocate device memory.  The source pages
+ * have no counterpart to this entry point: it exists only for code that must
+ * not call cudaMalloc (or any allocating routine) itself.
+ *
+ * Same operation, arguments and kernels as qmm_gemm, but the scratch qmm_gemm
+ * takes as `workspace` is a fixed array of QMM_BUILTIN_WORKSPACE_BYTES (8 MiB)
+ * compiled into the library and reserved on each device when the library's
+ * module loads.  The function itself allocates nothing.
+ *   - Size limit: qmm_gemm_workspace_bytes(qtype, od, K, nt) must not exceed
+ *     QMM_BUILTIN_WORKSPACE_BYTES (e.g. nt = 512 at K = 4096 needs 4.5 MiB;
+ *     nt = 512 at K = 14336 needs 15.75 MiB and is refused).  A larger problem
+ *     returns QMM_EWORKSPACE and launches nothing; use qmm_gemm with a
+ *     workspace of your own for it.
+ *   - Nothing in the array has to start at zero: the prepass rewrites every
+ *     entry a stored output depends on, and each call zeroes the remaining
+ *     padding entries of the last token tile itself.
+ *   - There is one array per device, shared by all calls on that device.
+ *     Calls whose work can overlap on the device (different streams, or
+ *     different host threads without ordering between them) race on it and
+ *     may produce wrong results: keep them ordered, e.g. on one stream.
+ *   - The first call on each device looks the array's address up (a CUDA
+ *     runtime query, cached afterwards).  If that first call is what does
+ *     this set-up, make it before any stream capture begins.
+ * Errors: as qmm_gemm, plus QMM_EWORKSPACE for the size limit above and
+ * QMM_EDEVICE if the address lookup fails.
+ */
+#define QMM_BUILTIN_WORKSPACE_BYTES (8u << 20)
+int qmm_gemm_builtin_workspace(int qtype, const void *W, const int8_t *xq, const float *xds, float *out,
+                               int64_t od, int64_t K, int64_t nt, void *stream);
+
+/*
  * The whole method from f32 activations, all on `stream` ([CH04] sec. 3.3:
  * the small-batch / prefill split by nt):
  *   - Q4_K with nt*K small enough (nt <= 4, nt*round_up(K, 2048) <= 16384,

@@ -39,6 +39,7 @@ QMM_ETIMEOUT = -8
 QMM_EDEVICE = -9
 
 QMM_FLAG_STATIC_WEIGHTS = 1
+QMM_BUILTIN_WORKSPACE_BYTES = 8 << 20
 
 QMM_PATH_FUSED_MMVQ = 1
 QMM_PATH_MMVQ = 2
@@ -74,6 +75,9 @@ _SIGS = {
     "qmm_gemm": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "qmm_gemm_builtin_workspace": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                  ctypes.c_void_p]),
     "qmm_matmul": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint,
@@ -137,6 +141,8 @@ def qmm_gemv(qtype, W, xq, xds, out, od, K, nt, stream):
     return _call("qmm_gemv", qtype, W, xq, xds, out, od, K, nt, stream)
 def qmm_gemm(qtype, W, xq, xds, out, od, K, nt, workspace, ws_bytes, stream):
     return _call("qmm_gemm", qtype, W, xq, xds, out, od, K, nt, workspace, ws_bytes, stream)
+def qmm_gemm_builtin_workspace(qtype, W, xq, xds, out, od, K, nt, stream):
+    return _call("qmm_gemm_builtin_workspace", qtype, W, xq, xds, out, od, K, nt, stream)
 def qmm_matmul(qtype, W, x, xq, xds, out, od, K, nt, workspace, ws_bytes, flags, stream):
     return _call("qmm_matmul", qtype, W, x, xq, xds, out, od, K, nt, workspace, ws_bytes, flags, stream)
 def qmm_debug_block_dots(qtype, W, xq, xds, od, K, nt, dots, path, workspace, ws_bytes, stream):

@@ -270,3 +270,59 @@ const char* qmm_strerror(int status) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------- GEMM with a built-in workspace --
+// For callers that may not allocate device memory at all: the scratch the
+// tensor-core GEMM needs (f16 codes and token-contiguous scale rows) lives in
+// one fixed array that is part of the loaded module.  Its device address is
+// taken once per device and passed to the same prepass and GEMM kernels that
+// qmm_gemm runs on a caller's workspace.
+namespace qmm {
+namespace {
+
+static __device__ __align__(256) uint8_t g_builtin_ws[QMM_BUILTIN_WORKSPACE_BYTES];
+void* g_builtin_ws_ptr[kMaxDevices] = {};
+
+int builtin_ws_ptr(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMM_EDEVICE;
+  if (!g_builtin_ws_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_builtin_ws) != cudaSuccess || !p) return QMM_EDEVICE;
+    g_builtin_ws_ptr[dev] = p;
+  }
+  *out = g_builtin_ws_ptr[dev];
+  return QMM_OK;
+}
+
+}  // namespace
+}  // namespace qmm
+
+extern "C" int qmm_gemm_builtin_workspace(int qtype, const void* W, const int8_t* xq, const float* xds, float* out,
+                                          int64_t od, int64_t K, int64_t nt, void* stream) {
+  if (!valid_qtype(qtype)) return QMM_EINVAL_QTYPE;
+  if (!W || !xq || !xds || !out) return QMM_ENULL;
+  int rc = check_shape(od, K, nt);
+  if (rc) return rc;
+  if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
+  const size_t need = gemm_ws(nt, K);
+  if (need > (size_t)QMM_BUILTIN_WORKSPACE_BYTES) return QMM_EWORKSPACE;
+  rc = check_device();
+  if (rc) return rc;
+  void* ws = nullptr;
+  rc = builtin_ws_ptr(&ws);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The prepass writes the scale rows only for tokens < nt; the padding
+  // tokens of the last tile would otherwise hold whatever an earlier call of
+  // another shape left there.  They feed only output columns that are never
+  // stored, but they are zeroed so every call computes on defined values.
+  const int64_t ntp = gemm_ntp(nt);
+  if (ntp > nt) {
+    uint8_t* scl = static_cast<uint8_t*>(ws) + gemm_xh_bytes(nt, K);
+    if (cudaMemset2DAsync(scl + nt * 8, (size_t)ntp * 8, 0, (size_t)(ntp - nt) * 8, (size_t)(K / 32), st) !=
+        cudaSuccess)
+      return QMM_ELAUNCH;
+  }
+  return gemm_core(qtype, W, xq, xds, out, nullptr, od, K, nt, ws, (size_t)QMM_BUILTIN_WORKSPACE_BYTES, true, st);
+}
