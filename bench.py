@@ -181,6 +181,13 @@ def max_over_ranks(value: float, world: int, device=None):
     return float(t.item())
 
 
+def job_rate(world: int, units_per_rank_step: float, steps: int, ms_max: float, scale: float = 1e9) -> float:
+    """Whole-job throughput of N replicas: every rank processes the same units
+    per step, so the job's units are world * units * steps, over the slowest
+    rank's time (ms_max, already reduced with max_over_ranks)."""
+    return world * units_per_rank_step * steps / (ms_max / 1e3) / scale
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -316,8 +323,8 @@ def run_gpu(args):
     barrier(world)
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(ms, world, dev)
-    value = world * wbytes * args.steps / (ms_max / 1e3) / 1e9
-    tops = world * 2 * macs * args.steps / (ms_max / 1e3) / 1e12
+    value = job_rate(world, wbytes, args.steps, ms_max)
+    tops = job_rate(world, 2 * macs, args.steps, ms_max, 1e12)
     clocks = clk.summary()
     assert qmm.qmm_sync_status(st) == qmm.QMM_OK
 
@@ -395,7 +402,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
-    e2e = {"value": world * wbytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+    e2e = {"value": job_rate(world, wbytes, 1, e2e_ms), "unit": "GB/s",
            "h2d_bytes_per_step": sum(cc.nt * cc.K * 4 for cc in cases),
            "d2h_bytes_per_step": sum(cc.nt * cc.od * 4 for cc in cases), "ms_per_step": e2e_ms}
 
