@@ -10,8 +10,8 @@ projection), through the C ABI.
 value   weight GB/s of the whole job: weight bytes of all steps on all ranks /
         max-over-ranks wall time of the timed region, inputs resident in HBM.
         Each step reads the next of 16 rotating weight copies (557 MB > 4x L2),
-        so no step finds its weights in L2.  The steps are replayed as one
-        CUDA graph per copy.
+        so no step finds its weights in L2.  The steps are replayed from a
+        CUDA graph of 16 consecutive steps.
 e2e     the same metric with the activations copied from pinned host memory and
         the outputs copied back inside every step, one qmm_matmul call per
         projection from Python.
@@ -291,22 +291,34 @@ def run_gpu(args):
             if rc != qmm.QMM_OK:
                 raise qmm.QmmError(rc, "qmm_matmul")
 
-    # warm up eagerly once (first-call set-up happens outside any capture), then capture
+    # warm up eagerly once (first-call set-up happens outside any capture), then
+    # capture: one graph runs NCOPIES consecutive steps (one per weight copy),
+    # so consecutive matmuls stay programmatic dependents of each other across
+    # steps; single-step graphs cover a remainder of K mod NCOPIES steps
     with torch.cuda.stream(stream):
         step(0)
     stream.synchronize()
-    graphs = []
-    for k in range(NCOPIES):
+
+    def capture(copies):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step(k, torch.cuda.current_stream().cuda_stream)
-        graphs.append(g)
+            for k in copies:
+                step(k, torch.cuda.current_stream().cuda_stream)
+        return g
+
+    g_all = capture(range(NCOPIES))
+    g_one = [capture([k]) for k in range(NCOPIES)]
     torch.cuda.synchronize()
     assert qmm.qmm_sync_status(st) == qmm.QMM_OK
 
+    def run_steps(n):
+        for _ in range(n // NCOPIES):
+            g_all.replay()
+        for k in range(n % NCOPIES):
+            g_one[k].replay()
+
     with torch.cuda.stream(stream):
-        for w in range(args.warmup):
-            graphs[w % NCOPIES].replay()
+        run_steps(args.warmup)
     torch.cuda.synchronize()
 
     # ---- timed region: exactly K steps
@@ -316,8 +328,7 @@ def run_gpu(args):
     with ClockSampler(local_rank) as clk:
         with torch.cuda.stream(stream):
             ev0.record(stream)
-            for s in range(args.steps):
-                graphs[s % NCOPIES].replay()
+            run_steps(args.steps)
             ev1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -425,7 +436,7 @@ def run_gpu(args):
                        "qtype": "Q4_K", "x": "N(0,1) + 0.1% x20 outliers", "seed": 0,
                        "parallelism": f"replicas x{world}",
                        "l2": f"{NCOPIES} rotating weight copies ({NCOPIES * wbytes / 1e6:.0f} MB > L2)",
-                       "graphs": "one CUDA graph per step"},
+                       "graphs": f"CUDA graph of {NCOPIES} consecutive steps"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
         }

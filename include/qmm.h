@@ -102,10 +102,12 @@ int qmm_gemv_max_nt(void);
 
 /*
  * q8_1 quantization of x [nt][K] f32 ([MOJO] "The GPU path"; [CH04]
- * sec. 3.4).  One warp per 32-value block, one value per lane: amax by a
- * shuffle max, d = amax/127 (IEEE f32 division), q = round-half-even(x/d)
- * clamped to [-127, 127], s = d * (float)sum(q) with sum(q) an integer
- * shuffle sum.  A block of zeros gives d = s = 0 and q = 0.
+ * sec. 3.4).  Per 32-value block: amax by a shuffle max, d = amax/127 (IEEE
+ * f32 division), q = round-half-even of the IEEE quotient x/d clamped to
+ * [-127, 127], s = d * (float)sum(q) with sum(q) an integer shuffle sum.  The
+ * codes are decided from x * fl(1/d) and fall back to the division only when
+ * that lands within 1e-4 of a half-integer, so they equal the division's.  A
+ * block of zeros gives d = s = 0 and q = 0.
  * Output: xq [nt][K] int8, xds [nt][K/32][2] f32 (d, s).  K % 32 == 0
  * suffices here.  Bit-exact with the IEEE definition.
  */

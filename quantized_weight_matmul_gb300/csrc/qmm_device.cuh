@@ -162,6 +162,51 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// q8_1 codes of four values of one 32-value block whose scale is
+// d = fl(amax/127): q = round-half-even(fl(x/d)), clamped to [-127, 127] --
+// the IEEE quotient rounded to the nearest integer -- without a division per
+// value.  With r = fl(1/d), y = fl(x*r) is within |x/d| * 2^-23 < 1.6e-5 of
+// x/d (|x/d| <= 127.00001), and fl(x/d) within 2^-24 * |x/d| < 7.6e-6 of it,
+// so when y is more than 1e-4 away from every half-integer, y and fl(x/d) lie
+// inside the same rounding interval and rint(y) is the code.  When any lane
+// of the warp has a value that close to a half-integer (or 1/d overflows), the
+// whole warp takes the correctly rounded division instead.  All 32 lanes of
+// the warp must call this together.
+__device__ __forceinline__ void q8_codes4(const float (&v)[4], float d, int (&q)[4]) {
+  bool exact = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = 0;
+  if (d != 0.0f) {
+    const float r = __frcp_rn(d);
+    exact = !(r < INFINITY);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float y = v[i] * r;
+      const float n = rintf(y);
+      exact |= fabsf(fabsf(y - n) - 0.5f) <= 1e-4f;
+      q[i] = max(-127, min(127, (int)n));
+    }
+  }
+  if (__any_sync(0xffffffffu, exact) && d != 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], d))));
+  }
+}
+
+// Pull one 2-D tile of a tensor map into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+               : "memory");
+}
+
+// Dot product of the four unsigned bytes of a with the four signed bytes of b,
+// plus c.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -95,6 +95,10 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+__device__ __forceinline__ void named_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 template <int NT, int NW, int R, bool DOTS, bool FUSED>
 __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
     gemv_q4k_stream_kernel(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ x,
@@ -170,6 +174,12 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
           seg = 0;
           ++grp;
         }
+        if (c == stages - 1) {
+          // the ring is full: pull the rest of this CTA's weights into L2 now,
+          // so the refills of the ring are L2 hits
+          for (int c2 = stages; c2 < nchunks; ++c2)
+            tma_prefetch_l2_2d(&tmW, (c2 % nseg) * (kSegBytes / 8), (g_begin + c2 / nseg) * C::CR);
+        }
       }
       if (!act_issued) {
         griddep_wait();
@@ -192,31 +202,46 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
     // ----------------------------------------------------------- consumers
     const int sbo = lane >> 2, p = lane & 3;
     bool ok = true;
-    griddep_wait();  // the preceding grid is complete before this thread reads x or writes
+    // the preceding grid is complete before any consumer reads x or writes:
+    // one warp waits for it, the others sleep on a named barrier meanwhile
+    if (warp == 0) {
+      griddep_wait();
+      named_arrive(2, 32 * NW);
+    } else {
+      named_barrier(2, 32 * NW);
+    }
     if (FUSED) {
       // q8_1 of x [NT][K] into shared memory: eight lanes per 32-value block,
       // four values per lane; block maximum and code sum by shuffles within
       // the eight lanes; d = amax/127 and q = round-half-even(x/d) by IEEE
       // division, s = d*(float)sum(q).  CTA (b mod grid) also writes block b
       // of the xq / xds outputs.
-      const int nblk = NT * (K >> 5);
+      const int nblk = NT * (K >> 5), nbk = K >> 5;
       const int q8 = lane & 7;
-      for (int base = warp * 4; base < nblk; base += NW * 4) {
-        const int b = base + (lane >> 3);
+      constexpr int QJ = (int)(kFusedMaxAct / (4 * 32 * NW));
+      const int tid = warp * 32 + lane;
+      const int nf4 = NT * K / 4;
+      // every load of this thread is issued before any is used
+      float4 xv[QJ];
+#pragma unroll
+      for (int j = 0; j < QJ; ++j) {
+        const int f = tid + 32 * NW * j;
+        xv[j] = f < nf4 ? __ldg(reinterpret_cast<const float4*>(x) + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      int b = tid >> 3;  // block of step j is b + 4 * NW * j: token t, block kb within the token
+      int t = b / nbk, kb = b - t * nbk;
+#pragma unroll
+      for (int j = 0; j < QJ; ++j) {
+        if (32 * NW * j >= nf4) break;
         const bool in = b < nblk;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (in) v = __ldg(reinterpret_cast<const float4*>(x + (size_t)b * 32 + q8 * 4));
-        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        const float vv[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        float amax = fmaxf(fmaxf(fabsf(vv[0]), fabsf(vv[1])), fmaxf(fabsf(vv[2]), fabsf(vv[3])));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
         const float d = __fdiv_rn(amax, 127.0f);
-        int q[4] = {0, 0, 0, 0};
-        if (d != 0.0f) {
-          const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) q[i] = max(-127, min(127, __float2int_rn(__fdiv_rn(vv[i], d))));
-        }
+        int q[4];
+        q8_codes4(vv, d, q);
         int sum = q[0] + q[1] + q[2] + q[3];
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -225,13 +250,18 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         const uint32_t packed = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
                                 ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
         if (in) {
-          const int t = b / (K >> 5), k = (b % (K >> 5)) * 32 + q8 * 4;
-          *reinterpret_cast<uint32_t*>(sx + t * Kp + fused_code_offset(k)) = packed;
+          *reinterpret_cast<uint32_t*>(sx + t * Kp + fused_code_offset(kb * 32 + q8 * 4)) = packed;
           if (q8 == 0) *reinterpret_cast<float2*>(sds + 2 * b) = make_float2(d, s);
-          if (b % gridDim.x == blockIdx.x) {
+          if (blockIdx.x == 0) {  // one CTA writes the q8_1 outputs
             *reinterpret_cast<uint32_t*>(xq + (size_t)b * 32 + q8 * 4) = packed;
             if (q8 == 0) reinterpret_cast<float2*>(xds)[b] = make_float2(d, s);
           }
+        }
+        b += 4 * NW;
+        kb += 4 * NW;
+        while (kb >= nbk) {
+          kb -= nbk;
+          ++t;
         }
       }
       named_barrier(1, 32 * NW);
@@ -273,13 +303,13 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           lo[i][k] = w[k] & 0x0F0F0F0Fu;
-          hi[i][k] = (w[k] >> 4) & 0x0F0F0F0Fu;
+          hi[i][k] = w[k] & 0xF0F0F0F0u;  // 16 x the high nibbles: one AND instead of a shift and an AND
         }
         uint32_t sc2, m2;
         q4k_pair_codes(hdr.y, hdr.z, hdr.w, p, sc2, m2);
         const float d = half_bits_to_float(hdr.x), dmin = half_bits_to_float(hdr.x >> 16);
         a_lo[i] = d * (float)(sc2 & 0xFFu);
-        a_hi[i] = d * (float)(sc2 >> 8);
+        a_hi[i] = d * (float)(sc2 >> 8) * 0.0625f;  // the high-nibble dot comes out 16x (exact power of 2)
         c_lo[i] = dmin * (float)(m2 & 0xFFu);
         c_hi[i] = dmin * (float)(m2 >> 8);
       }
@@ -310,13 +340,13 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               dlo = __dp4a((int)lo[i][k], (int)xw[k], dlo);
-              dhi = __dp4a((int)hi[i][k], (int)yw[k], dhi);
+              dhi = dp4a_us(hi[i][k], yw[k], dhi);
             }
             if constexpr (DOTS) {
               if (row0 + i < od) {
                 int32_t* dst = dots + ((size_t)t * od + row0 + i) * (K >> 5) + jlo;
                 dst[0] = dlo;
-                dst[1] = dhi;
+                dst[1] = dhi >> 4;  // a multiple of 16: exact
               }
             } else {
               float a = acc[i][t];

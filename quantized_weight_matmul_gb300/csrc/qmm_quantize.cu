@@ -1,10 +1,10 @@
 // qmm_quantize.cu -- q8_1 activation quantizer and the tensor-core GEMM's
 // activation-operand prepass.
 //
-// q8_1 ("The quantized GEMM", mojo-dllm, section "The GPU path"): one warp per
-// 32-value block, one value per lane; the block maximum |x| and the integer
-// sum of the codes are warp-shuffle reductions; the scale d = amax/127 and the
-// code q = round-half-even(x/d) use IEEE f32 division; s = d * sum(q).
+// q8_1 ("The quantized GEMM", mojo-dllm, section "The GPU path"): per
+// 32-value block the maximum |x| and the integer sum of the codes are
+// warp-shuffle reductions; d = amax/127 by IEEE f32 division; the code is
+// round-half-even of the IEEE quotient x/d; s = d * sum(q).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -13,7 +13,11 @@
 
 namespace qmm {
 
-// One warp per 32-value block; grid-stride over all nt*K/32 blocks.
+// Eight lanes per 32-value block, four values per lane (one 16-byte load);
+// a warp takes four blocks per step, grid-stride over all nt*K/32 blocks.
+// The block maximum and the code sum are 3-step shuffle reductions within the
+// eight lanes; d = amax/127 by IEEE division, the codes by q8_codes4 (the
+// same integers IEEE division and round-half-even give), s = d * sum(q).
 // When xh / scl are non-null the same pass also writes the tensor-core GEMM
 // operands: the codes as exact f16 (xh [nt][K]) and the scales token-
 // contiguous (scl [K/32][ntp] float2 = (d, s)).
@@ -22,33 +26,47 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restr
                                                             float2* __restrict__ xds,
                                                             __half* __restrict__ xh,
                                                             float2* __restrict__ scl, int64_t ntp) {
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, q8 = lane & 7;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   // wait until the preceding grid is done (it may write x or read xq / xds),
   // then let the next kernel -- the matmul -- start streaming its weights:
   // everything enqueued before this grid is complete at that point
   griddep_wait();
   griddep_launch_dependents();
-  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nblocks; b += warps) {
-    const float v = __ldg(x + b * 32 + lane);
-    float amax = fabsf(v);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  for (int64_t b0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4; b0 < nblocks;
+       b0 += warps * 4) {
+    const int64_t b = b0 + (lane >> 3);
+    const bool in = b < nblocks;
+    const float4 v4 = in ? __ldg(reinterpret_cast<const float4*>(x + b * 32) + q8) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const float d = __fdiv_rn(amax, 127.0f);
-    int q = 0;
-    if (d != 0.0f) {
-      q = __float2int_rn(__fdiv_rn(v, d));
-      q = max(-127, min(127, q));
-    }
-    xq[b * 32 + lane] = (int8_t)q;
-    const int sum = __reduce_add_sync(0xffffffffu, q);
+    int q[4];
+    q8_codes4(v, d, q);
+    int sum = q[0] + q[1] + q[2] + q[3];
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
     const float s = __fmul_rn(d, (float)sum);
-    if (xh) xh[b * 32 + lane] = __int2half_rn(q);
-    if (lane == 0) {
-      xds[b] = make_float2(d, s);
-      if (scl) {
-        const int64_t t = b / nb_per_row, j = b % nb_per_row;
-        scl[j * ntp + t] = make_float2(d, s);
+    if (in) {
+      *reinterpret_cast<uint32_t*>(xq + b * 32 + 4 * q8) = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
+                                                            ((uint32_t)(q[2] & 0xFF) << 16) |
+                                                            ((uint32_t)(q[3] & 0xFF) << 24);
+      if (xh) {
+        const __half2 h01 = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
+        const __half2 h23 = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
+        *reinterpret_cast<uint2*>(xh + b * 32 + 4 * q8) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+      }
+      if (q8 == 0) {
+        xds[b] = make_float2(d, s);
+        if (scl) {
+          const int64_t t = b / nb_per_row, j = b % nb_per_row;
+          scl[j * ntp + t] = make_float2(d, s);
+        }
       }
     }
   }
@@ -100,7 +118,7 @@ int launch_quantize(const float* x, int64_t nt, int64_t K, int8_t* xq, float* xd
                     float* scl, int64_t ntp, cudaStream_t stream) {
   const int64_t nblocks = nt * (K / 32);
   if (nblocks == 0) return QMM_OK;
-  return launch_ex(quantize_q8_1_kernel, dim3(grid_for(nblocks, 8)), dim3(256), 0, stream, true, x, nblocks,
+  return launch_ex(quantize_q8_1_kernel, dim3(grid_for(nblocks, 32)), dim3(256), 0, stream, true, x, nblocks,
                     (int64_t)(K / 32), xq, reinterpret_cast<float2*>(xds), xh, reinterpret_cast<float2*>(scl),
                     ntp);
 }

@@ -50,6 +50,47 @@ def test_quantize_bit_exact(nt, K, outliers):
     assert np.array_equal(xds.cpu().numpy().view(np.uint32), ods.view(np.uint32))
 
 
+def _near_tie_blocks(K=4096, seed=7):
+    """One token of K values whose quotients x/d sit on, or a few ulps beside,
+    half-integers -- where the rounding of the IEEE quotient is decided -- plus
+    a block whose scale is subnormal (its reciprocal overflows) and a zero
+    block."""
+    rng = np.random.default_rng(seed)
+    x = np.zeros(K, dtype=np.float32)
+    nb = K // 32
+    for b in range(nb - 2):
+        amax = np.float32(rng.choice([127.0, 100.0, 3.7, 1e-3, 55.5]) * rng.uniform(0.5, 2.0))
+        d = np.float32(amax / np.float32(127.0))
+        blk = np.empty(32, dtype=np.float32)
+        blk[0] = amax if b % 2 else -amax
+        for i in range(1, 32):
+            h = np.float32(rng.integers(-126, 126) + 0.5)
+            v = np.float32(h * d)
+            steps = int(rng.integers(-3, 4))  # 0: on the tie's product; else a few ulps aside
+            for _ in range(abs(steps)):
+                v = np.nextafter(v, np.float32(np.inf) if steps > 0 else np.float32(-np.inf), dtype=np.float32)
+            blk[i] = v if abs(v) <= amax else np.float32(h * d)
+        x[32 * b:32 * (b + 1)] = blk
+    x[32 * (nb - 2):32 * (nb - 1)] = np.float32(1e-40) * np.arange(-16, 16, dtype=np.float32)  # subnormal scale
+    return x[None, :]  # last block stays zero
+
+
+def test_quantize_near_ties_bit_exact():
+    """Values whose quotients lie on or within a few ulps of a rounding
+    boundary: the quantizer and the fused decode kernel give the IEEE codes."""
+    x = _near_tie_blocks()
+    oq, ods = ora().quantize_q8_1(x)
+    xq, xds = qmm.quantize_q8_1(dev(x, torch))
+    assert np.array_equal(xq.cpu().numpy(), oq)
+    assert np.array_equal(xds.cpu().numpy().view(np.uint32), ods.view(np.uint32))
+    # the fused quantize + MMVQ route writes the same codes
+    W, _ = synth.Case(Q4_K, 256, x.shape[1], 1).generate()
+    assert qmm.qmm_matmul_path(Q4_K, 256, x.shape[1], 1) == qmm.QMM_PATH_FUSED_MMVQ
+    _, fq, fds = qmm.matmul(Q4_K, dev(W, torch), dev(x, torch), 256, return_q8=True)
+    assert np.array_equal(fq.cpu().numpy(), oq)
+    assert np.array_equal(fds.cpu().numpy().view(np.uint32), ods.view(np.uint32))
+
+
 # ------------------------------------------------------------ block dots ---
 
 @pytest.mark.parametrize("od,K,nt", [(256, 512, 1), (256, 512, 8), (1000, 768, 3), (64, 14336, 2),
