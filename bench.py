@@ -460,8 +460,13 @@ def run_sweep(args):
     st = stream.cuda_stream
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     names = args.families.split(",") if args.families else list(synth.WORKLOADS)
-    for fam in names:
-        for c in synth.WORKLOADS[fam].cases:
+    fams = [(fam, synth.WORKLOADS[fam].cases) for fam in names]
+    if args.shape:  # e.g. Q4_K:44032x4096x1 -- one extra case, seeded like the others
+        qt, dims = args.shape.split(":")
+        od_, K_, nt_ = (int(v) for v in dims.split("x"))
+        fams = [("shape", [synth.Case({"Q4_K": synth.Q4_K, "Q6_K": synth.Q6_K}[qt], od_, K_, nt_)])]
+    for fam, fcases in fams:
+        for c in fcases:
             if args.case and c.name != args.case:
                 continue
             W, x = c.generate()
@@ -542,6 +547,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--families", default="")
     ap.add_argument("--case", default="", help="sweep: only the case with this name")
+    ap.add_argument("--shape", default="", help="sweep: one case of this shape instead, QTYPE:ODxKxNT")
     ap.add_argument("--reps", type=int, default=0, help="sweep: timed launches per case")
     ap.add_argument("--copies", type=int, default=0, help="sweep: rotating weight copies per case")
     ap.add_argument("--no-graph", action="store_true", help="sweep: launch from Python instead of a CUDA graph")

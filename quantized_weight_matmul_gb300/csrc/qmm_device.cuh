@@ -162,41 +162,39 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// q8_1 codes of four values of one 32-value block whose scale is
+// q8_1 codes of N values of one 32-value block whose scale is
 // d = fl(amax/127): q = round-half-even(fl(x/d)), clamped to [-127, 127] --
 // the IEEE quotient rounded to the nearest integer -- without a division per
 // value.  With r = fl(1/d), y = fl(x*r) is within |x/d| * 2^-23 < 1.6e-5 of
 // x/d (|x/d| <= 127.00001), and fl(x/d) within 2^-24 * |x/d| < 7.6e-6 of it,
 // so when y is more than 1e-4 away from every half-integer, y and fl(x/d) lie
-// inside the same rounding interval and rint(y) is the code.  When any lane
-// of the warp has a value that close to a half-integer (or 1/d overflows), the
-// whole warp takes the correctly rounded division instead.  All 32 lanes of
-// the warp must call this together.
-__device__ __forceinline__ void q8_codes4(const float (&v)[4], float d, int (&q)[4]) {
-  bool exact = false;
+// inside the same rounding interval and rint(y) is the code.  A value that
+// close to a half-integer (or every value, when 1/d overflows) takes the
+// correctly rounded division instead; the warp votes first so that the
+// divisions run only when some lane needs one.  All 32 lanes of the warp must
+// call this together.
+template <int N>
+__device__ __forceinline__ void q8_codes(const float (&v)[N], float d, int (&q)[N]) {
+  static_assert(N <= 32, "one bit per value");
+  uint32_t near = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) q[i] = 0;
+  for (int i = 0; i < N; ++i) q[i] = 0;
   if (d != 0.0f) {
     const float r = __frcp_rn(d);
-    exact = !(r < INFINITY);
+    if (!(r < INFINITY)) near = N == 32 ? 0xFFFFFFFFu : (1u << N) - 1u;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < N; ++i) {
       const float y = v[i] * r;
       const float n = rintf(y);
-      exact |= fabsf(fabsf(y - n) - 0.5f) <= 1e-4f;
+      if (fabsf(fabsf(y - n) - 0.5f) <= 1e-4f) near |= 1u << i;
       q[i] = max(-127, min(127, (int)n));
     }
   }
-  if (__any_sync(0xffffffffu, exact) && d != 0.0f) {
+  if (__any_sync(0xffffffffu, near != 0)) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], d))));
+    for (int i = 0; i < N; ++i)
+      if (near & (1u << i)) q[i] = max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], d))));
   }
-}
-
-// Pull one 2-D tile of a tensor map into L2 (no shared-memory destination).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
-               : "memory");
 }
 
 // Dot product of the four unsigned bytes of a with the four signed bytes of b,

@@ -22,9 +22,9 @@
 //   * staged: q8_1 codes and scales produced by the quantizer are copied
 //     once per CTA into shared memory (bulk copy);
 //   * fused: the consumer warps quantize the f32 activations themselves into
-//     shared memory (the same IEEE arithmetic as the quantizer, so the codes
-//     are bit-identical) and write the q8_1 outputs too -- one kernel per
-//     matmul instead of two, for the decode shapes where nt*K is small.
+//     shared memory (two lanes per 32-value block; the same codes as the
+//     quantizer, see q8_codes) and write the q8_1 outputs too -- one kernel
+//     per matmul instead of two, for the decode shapes where nt*K is small.
 // Kernels are launched as programmatic dependents of the preceding kernel
 // and let their own dependents start early, so consecutive matmuls overlap
 // their launch and ramp.  Every global access that may depend on the
@@ -174,12 +174,6 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
           seg = 0;
           ++grp;
         }
-        if (c == stages - 1) {
-          // the ring is full: pull the rest of this CTA's weights into L2 now,
-          // so the refills of the ring are L2 hits
-          for (int c2 = stages; c2 < nchunks; ++c2)
-            tma_prefetch_l2_2d(&tmW, (c2 % nseg) * (kSegBytes / 8), (g_begin + c2 / nseg) * C::CR);
-        }
       }
       if (!act_issued) {
         griddep_wait();
@@ -217,51 +211,53 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
       // division, s = d*(float)sum(q).  CTA (b mod grid) also writes block b
       // of the xq / xds outputs.
       const int nblk = NT * (K >> 5), nbk = K >> 5;
-      const int q8 = lane & 7;
-      constexpr int QJ = (int)(kFusedMaxAct / (4 * 32 * NW));
-      const int tid = warp * 32 + lane;
-      const int nf4 = NT * K / 4;
-      // every load of this thread is issued before any is used
-      float4 xv[QJ];
-#pragma unroll
-      for (int j = 0; j < QJ; ++j) {
-        const int f = tid + 32 * NW * j;
-        xv[j] = f < nf4 ? __ldg(reinterpret_cast<const float4*>(x) + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      int b = tid >> 3;  // block of step j is b + 4 * NW * j: token t, block kb within the token
-      int t = b / nbk, kb = b - t * nbk;
-#pragma unroll
-      for (int j = 0; j < QJ; ++j) {
-        if (32 * NW * j >= nf4) break;
+      const int tid = warp * 32 + lane, half = lane & 1;
+      // two lanes per 32-value block, sixteen values (four 16-byte loads) each:
+      // the decode shapes (nt = 1, K <= 4096) take a single pass
+      for (int it = 0; it * 16 * NW < nblk; ++it) {
+        const int b = it * 16 * NW + (tid >> 1);
         const bool in = b < nblk;
-        const float vv[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-        float amax = fmaxf(fmaxf(fabsf(vv[0]), fabsf(vv[1])), fmaxf(fabsf(vv[2]), fabsf(vv[3])));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-        const float d = __fdiv_rn(amax, 127.0f);
-        int q[4];
-        q8_codes4(vv, d, q);
-        int sum = q[0] + q[1] + q[2] + q[3];
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        const float s = __fmul_rn(d, (float)sum);
-        const uint32_t packed = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
-                                ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
-        if (in) {
-          *reinterpret_cast<uint32_t*>(sx + t * Kp + fused_code_offset(kb * 32 + q8 * 4)) = packed;
-          if (q8 == 0) *reinterpret_cast<float2*>(sds + 2 * b) = make_float2(d, s);
-          if (blockIdx.x == 0) {  // one CTA writes the q8_1 outputs
-            *reinterpret_cast<uint32_t*>(xq + (size_t)b * 32 + q8 * 4) = packed;
-            if (q8 == 0) reinterpret_cast<float2*>(xds)[b] = make_float2(d, s);
-          }
+        const float4* src = reinterpret_cast<const float4*>(x + (size_t)b * 32 + 16 * half);
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 t4 = in ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[4 * i] = t4.x;
+          v[4 * i + 1] = t4.y;
+          v[4 * i + 2] = t4.z;
+          v[4 * i + 3] = t4.w;
         }
-        b += 4 * NW;
-        kb += 4 * NW;
-        while (kb >= nbk) {
-          kb -= nbk;
-          ++t;
+        float m[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+#pragma unroll
+        for (int w2 = 4; w2 > 0; w2 >>= 1)
+#pragma unroll
+          for (int i = 0; i < w2; ++i) m[i] = fmaxf(m[i], m[i + w2]);
+        const float amax = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
+        const float d = __fdiv_rn(amax, 127.0f);
+        int q[16];
+        q8_codes<16>(v, d, q);
+        int sum = 0;
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          sum += q[4 * i] + q[4 * i + 1] + q[4 * i + 2] + q[4 * i + 3];
+          pk[i] = (uint32_t)(q[4 * i] & 0xFF) | ((uint32_t)(q[4 * i + 1] & 0xFF) << 8) |
+                  ((uint32_t)(q[4 * i + 2] & 0xFF) << 16) | ((uint32_t)(q[4 * i + 3] & 0xFF) << 24);
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        const float s = __fmul_rn(d, (float)sum);
+        if (in) {
+          // codes k..k+15 are one contiguous 16-byte chunk of the plane
+          const int t = b / nbk, kb = b - t * nbk;
+          *reinterpret_cast<uint4*>(sx + t * Kp + fused_code_offset(kb * 32 + 16 * half)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          if (half == 0) *reinterpret_cast<float2*>(sds + 2 * b) = make_float2(d, s);
+          if (blockIdx.x == 0) {  // one CTA writes the q8_1 outputs
+            *reinterpret_cast<uint4*>(xq + (size_t)b * 32 + 16 * half) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if (half == 0) reinterpret_cast<float2*>(xds)[b] = make_float2(d, s);
+          }
         }
       }
       named_barrier(1, 32 * NW);

@@ -16,7 +16,7 @@ namespace qmm {
 // Eight lanes per 32-value block, four values per lane (one 16-byte load);
 // a warp takes four blocks per step, grid-stride over all nt*K/32 blocks.
 // The block maximum and the code sum are 3-step shuffle reductions within the
-// eight lanes; d = amax/127 by IEEE division, the codes by q8_codes4 (the
+// eight lanes; d = amax/127 by IEEE division, the codes by q8_codes (the
 // same integers IEEE division and round-half-even give), s = d * sum(q).
 // When xh / scl are non-null the same pass also writes the tensor-core GEMM
 // operands: the codes as exact f16 (xh [nt][K]) and the scales token-
@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restr
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const float d = __fdiv_rn(amax, 127.0f);
     int q[4];
-    q8_codes4(v, d, q);
+    q8_codes<4>(v, d, q);
     int sum = q[0] + q[1] + q[2] + q[3];
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
