@@ -77,8 +77,10 @@ size_t qmm_weight_bytes(int qtype, int64_t od, int64_t K);
 size_t qmm_xq_bytes(int64_t nt, int64_t K);
 size_t qmm_xds_bytes(int64_t nt, int64_t K);
 
-/* Workspace qmm_gemm needs for this problem (f16 copy of the int8 codes and
- * token-contiguous scale planes, see qmm_gemm).  0 for invalid input. */
+/* Workspace qmm_gemm needs for this problem (f16 copy of the int8 codes,
+ * token-contiguous scale planes and, for shapes with fewer output tiles than
+ * SMs, split-K partial sums; see qmm_gemm).  A function of the shape alone.
+ * 0 for invalid input. */
 size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
 
 /* Workspace qmm_matmul needs: 0 on its MMVQ paths (Q4_K, nt <= 8), else
@@ -137,6 +139,10 @@ int qmm_gemv(int qtype, const void *W, const int8_t *xq, const float *xds, float
  * `workspace` (device, 16-byte aligned, >= qmm_gemm_workspace_bytes) holds
  * an f16 copy of xq and the scale planes written by a prepass on `stream`;
  * its contents need not be preserved between calls.  out is overwritten.
+ * When the 128-row x token tiles are fewer than the GPU's SMs, K is split
+ * into up to 8 slices of whole super-blocks computed by separate CTAs; their
+ * fp32 partial sums (in the workspace) are added in a fixed order, so
+ * results stay bitwise reproducible.
  */
 int qmm_gemm(int qtype, const void *W, const int8_t *xq, const float *xds, float *out,
              int64_t od, int64_t K, int64_t nt, void *workspace, size_t ws_bytes, void *stream);

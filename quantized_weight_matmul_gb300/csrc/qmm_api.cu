@@ -60,7 +60,10 @@ int check_device() {
   return cached[dev] == 1 ? QMM_OK : QMM_EDEVICE;
 }
 
-size_t gemm_ws(int64_t nt, int64_t K) { return gemm_xh_bytes(nt, K) + gemm_scl_bytes(nt, K); }
+// f16 codes, token-contiguous scale rows, then the split-K partial sums
+size_t gemm_ws(int64_t od, int64_t K, int64_t nt) {
+  return gemm_xh_bytes(nt, K) + gemm_scl_bytes(nt, K) + gemm_part_bytes(od, K, nt);
+}
 
 // The qmm_matmul route for a valid problem (one place, so the query below and
 // the dispatch cannot disagree).
@@ -72,7 +75,7 @@ int matmul_route(int qtype, int64_t nt, int64_t K) {
 
 int gemm_core(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
               int64_t od, int64_t K, int64_t nt, void* ws, size_t ws_bytes, bool prep, cudaStream_t st) {
-  if (ws_bytes < gemm_ws(nt, K)) return QMM_EWORKSPACE;
+  if (ws_bytes < gemm_ws(od, K, nt)) return QMM_EWORKSPACE;
   if (!ws) return QMM_ENULL;
   if (!aligned16(ws)) return QMM_EALIGN;
   if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
@@ -81,11 +84,12 @@ int gemm_core(int qtype, const void* W, const int8_t* xq, const float* xds, floa
   if (rc) return rc;
   __half* xh = static_cast<__half*>(ws);
   float* scl = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + gemm_xh_bytes(nt, K));
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + gemm_xh_bytes(nt, K) + gemm_scl_bytes(nt, K));
   if (prep) {
     rc = launch_gemm_prep(xq, xds, nt, K, gemm_ntp(nt), xh, scl, st);
     if (rc) return rc;
   }
-  return launch_gemm_tc(qtype, W, xh, scl, out, dots, od, K, nt, status, g_stall_ms.load(), st);
+  return launch_gemm_tc(qtype, W, xh, scl, out, dots, part, od, K, nt, status, g_stall_ms.load(), st);
 }
 
 }  // namespace
@@ -108,13 +112,13 @@ size_t qmm_xds_bytes(int64_t nt, int64_t K) {
 
 size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt) {
   if (!valid_qtype(qtype) || check_shape(od, K, nt)) return 0;
-  return gemm_ws(nt, K);
+  return gemm_ws(od, K, nt);
 }
 
 size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt) {
   if (!valid_qtype(qtype) || check_shape(od, K, nt)) return 0;
   if (matmul_route(qtype, nt, K) != QMM_PATH_MMQ) return 0;
-  return gemm_ws(nt, K);
+  return gemm_ws(od, K, nt);
 }
 
 int qmm_matmul_path(int qtype, int64_t od, int64_t K, int64_t nt) {
@@ -195,7 +199,7 @@ int qmm_matmul(int qtype, const void* W, const float* x, int8_t* xq, float* xds,
     if (rc) return rc;
     return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, status, true, st);
   }
-  if (ws_bytes < gemm_ws(nt, K)) return QMM_EWORKSPACE;
+  if (ws_bytes < gemm_ws(od, K, nt)) return QMM_EWORKSPACE;
   if (!workspace) return QMM_ENULL;
   if (!aligned16(workspace)) return QMM_EALIGN;
   if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
@@ -305,7 +309,7 @@ extern "C" int qmm_gemm_builtin_workspace(int qtype, const void* W, const int8_t
   int rc = check_shape(od, K, nt);
   if (rc) return rc;
   if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
-  const size_t need = gemm_ws(nt, K);
+  const size_t need = gemm_ws(od, K, nt);
   if (need > (size_t)QMM_BUILTIN_WORKSPACE_BYTES) return QMM_EWORKSPACE;
   rc = check_device();
   if (rc) return rc;

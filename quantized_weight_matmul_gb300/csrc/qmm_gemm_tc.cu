@@ -226,7 +226,11 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = blockIdx.x * C::BM, tok0 = blockIdx.y * BN;
-  const int nsb = K >> 8, NS = K >> 6;
+  // split-K: CTA z of gridDim.z takes super-blocks [b_off, b_off + nsb); all
+  // ring indices below are relative to the slice, addresses absolute
+  const int nsb_all = K >> 8, per = (nsb_all + (int)gridDim.z - 1) / (int)gridDim.z;
+  const int b_off = (int)blockIdx.z * per;
+  const int nsb = min(per, nsb_all - b_off), NS = 4 * nsb;
   const Guard g{abort_flag, status, global_ns() + (uint64_t)limit_ms * 1000000ull};
 
   if (threadIdx.x == 0) {
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(384, 1)
         if (!wait_bar(bars.raw_empty(rs), ((b / C::RS) & 1) ^ 1, g)) break;
         if (!(skip_first_weight_load && b == 0)) {
           mbar_arrive_expect_tx(bars.raw_full(rs), C::RAW_BYTES);
-          const int x = QT == kQ4 ? b * kQ4KBytes : (b * kQ6KBytes) & ~15;
+          const int x = QT == kQ4 ? (b + b_off) * kQ4KBytes : ((b + b_off) * kQ6KBytes) & ~15;
           tma_load_2d(raw_s + rs * C::RAW_BYTES, &tmW, x, row0, bars.raw_full(rs));
         }
         ++raw_issued;
@@ -289,10 +293,11 @@ __global__ void __launch_bounds__(384, 1)
             break;
           }
           mbar_arrive_expect_tx(bars.b_full(bs), (uint32_t)nbytes_b);
-          tma_load_2d(b_s + bs * C::B_BYTES, &tmX, C::KS * gs, tok0, bars.b_full(bs));
+          const int gk = gs + 4 * b_off;  // absolute 64-k stage
+          tma_load_2d(b_s + bs * C::B_BYTES, &tmX, C::KS * gk, tok0, bars.b_full(bs));
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi)
-            bulk_load(sc_s + bs * C::SC_BYTES + gi * BN * 8, scl + ((size_t)(2 * gs + gi) * ntp + tok0),
+            bulk_load(sc_s + bs * C::SC_BYTES + gi * BN * 8, scl + ((size_t)(2 * gk + gi) * ntp + tok0),
                       BN * 8, bars.b_full(bs));
           ++b_issued;
         }
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(384, 1)
           if (QT == kQ4)
             unpack_q4k_pair<!DOTS>(raw + r * C::RAW_ROW, s, a + r * 16);
           else
-            unpack_q6k_stage(raw + r * C::RAW_ROW, (b * kQ6KBytes) & 15, s, a + r * 16);
+            unpack_q6k_stage(raw + r * C::RAW_ROW, ((b + b_off) * kQ6KBytes) & 15, s, a + r * 16);
         }
         fence_proxy_async();
         __syncwarp();
@@ -380,7 +385,7 @@ __global__ void __launch_bounds__(384, 1)
     const int row_c = row_ok ? row_g : od - 1;
     constexpr int HALF = BN / 2;
     constexpr int CH = HALF / 32;
-    const size_t row_bytes = (size_t)nsb * (QT == kQ4 ? kQ4KBytes : kQ6KBytes);
+    const size_t row_bytes = (size_t)nsb_all * (QT == kQ4 ? kQ4KBytes : kQ6KBytes);
     const uint8_t* wrow = W + (size_t)row_c * row_bytes;
     float acc[HALF];
 #pragma unroll
@@ -388,42 +393,49 @@ __global__ void __launch_bounds__(384, 1)
     float sigma = 1.0f;  // acc holds (partial sum) / sigma
     int u = 0;
     bool ok = true;
+    // the next super-block's scale words are fetched one super-block ahead,
+    // so their global-load latency is off the epilogue's critical path
+    uint4 hdr_next = make_uint4(0, 0, 0, 0);  // Q4_K: d, dmin and the 12 packed scale bytes
+    uint32_t sw_next[9] = {};                 // Q6_K: the 16 int8 scales as 8 half-words, then d
+    auto fetch_scales = [&](int bb) {
+      if (DOTS || bb >= nsb) return;
+      if (QT == kQ4) {
+        hdr_next = __ldg(reinterpret_cast<const uint4*>(wrow + (size_t)(bb + b_off) * kQ4KBytes));
+      } else {
+        const uint16_t* hs = reinterpret_cast<const uint16_t*>(wrow + (size_t)(bb + b_off) * kQ6KBytes + 192);
+#pragma unroll
+        for (int i = 0; i < 9; ++i) sw_next[i] = __ldg(hs + i);
+      }
+    };
+    fetch_scales(0);
     for (int b = 0; b < nsb && ok; ++b) {
       float gcoef[QT == kQ4 ? 8 : 16];  // per-group coefficient (min term or scale)
       if (!DOTS) {
-        float d;
-        if (QT == kQ4) {
-          const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(wrow + (size_t)b * kQ4KBytes));
-          d = half_bits_to_float(hdr.x);
-          const float dmin = half_bits_to_float(hdr.x >> 16);
-          if (d != 0.0f) {
-            const float ratio = sigma / d;
-            sigma = d;
-            if (b > 0) {
+        const uint4 hdr = hdr_next;
+        uint32_t sw[9];
 #pragma unroll
-              for (int i = 0; i < HALF; ++i) acc[i] *= ratio;
-            }
+        for (int i = 0; i < 9; ++i) sw[i] = sw_next[i];
+        fetch_scales(b + 1);
+        // the rescaling factors only feed the fp32 sums, so a reciprocal
+        // within an ulp or two (instead of an IEEE division) is enough
+        const float d = half_bits_to_float(QT == kQ4 ? hdr.x : sw[8]);
+        if (d != 0.0f) {
+          const float ratio = sigma * __fdividef(1.0f, d);
+          sigma = d;
+          if (b > 0) {
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) acc[i] *= ratio;
           }
+        }
+        if (QT == kQ4) {
+          const float dmin_s = half_bits_to_float(hdr.x >> 16) * __fdividef(1.0f, sigma);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             int sc, m;
             q4k_scale_min_words(hdr.y, hdr.z, hdr.w, j, sc, m);
-            gcoef[j] = -(dmin * (float)m) / sigma;
+            gcoef[j] = -dmin_s * (float)m;
           }
         } else {
-          const uint16_t* hs = reinterpret_cast<const uint16_t*>(wrow + (size_t)b * kQ6KBytes + 192);
-          uint32_t sw[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) sw[i] = __ldg(hs + i);
-          d = half_bits_to_float(__ldg(hs + 8));
-          if (d != 0.0f) {
-            const float ratio = sigma / d;
-            sigma = d;
-            if (b > 0) {
-#pragma unroll
-              for (int i = 0; i < HALF; ++i) acc[i] *= ratio;
-            }
-          }
 #pragma unroll
           for (int gg = 0; gg < 16; ++gg) {
             const int sc = (int)(int8_t)((sw[gg >> 1] >> (8 * (gg & 1))) & 0xFF);
@@ -455,7 +467,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int c = 0; c < CH; ++c) tc_wait_ld(P[c]);
           if (DOTS) {
             const int ng = QT == kQ4 ? (K >> 5) : (K >> 4);
-            const int grp = QT == kQ4 ? 8 * b + 2 * s + gi : 16 * b + 4 * s + gi;
+            const int grp = QT == kQ4 ? 8 * (b + b_off) + 2 * s + gi : 16 * (b + b_off) + 4 * s + gi;
 #pragma unroll
             for (int c = 0; c < CH; ++c)
 #pragma unroll
@@ -497,7 +509,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int i = 0; i < HALF; ++i) {
         const int t = tok0 + hc * HALF + i;
-        if (t < nt) out[(size_t)t * od + row_g] = sigma * acc[i];
+        if (t < nt) out[((size_t)blockIdx.z * nt + t) * od + row_g] = sigma * acc[i];  // slice z's partials
       }
     }
   }
@@ -538,9 +550,20 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// out[i] = sum over the slices z = 0..S-1 of part[z][i], in that order.
+__global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restrict__ part, int S, int64_t n,
+                                                           float* __restrict__ out) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    float a = part[i];
+    for (int z = 1; z < S; ++z) a += part[(size_t)z * n + i];
+    out[i] = a;
+  }
+}
+
 template <int QT, int BN, bool DOTS>
-int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, int32_t* dots, int64_t od,
-               int64_t K, int64_t nt, int* status, int stall_ms, cudaStream_t stream) {
+int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, int32_t* dots, float* part,
+               int64_t od, int64_t K, int64_t nt, int* status, int stall_ms, cudaStream_t stream) {
   using C = Cfg<QT, BN>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QMM_EDEVICE;
@@ -562,33 +585,44 @@ int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, in
   if (!make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, (uint64_t)K, (uint64_t)nt, (uint64_t)K * 2, 64,
                    (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return QMM_ELAUNCH;
-  const dim3 grid((unsigned)((od + C::BM - 1) / C::BM), (unsigned)((nt + BN - 1) / BN));
+  // the block-dot hook writes every group once and needs no slicing
+  const int S = DOTS ? 1 : gemm_splits(od, K, nt);
+  if (S > 1 && !part) return QMM_EWORKSPACE;
+  const dim3 grid((unsigned)((od + C::BM - 1) / C::BM), (unsigned)((nt + BN - 1) / BN), (unsigned)S);
   const int limit_ms = stall_ms > 0 ? stall_ms : 4000;
   gemm_tc_kernel<QT, BN, DOTS><<<grid, 384, C::SMEM, stream>>>(
-      mw, mx, reinterpret_cast<const float2*>(scl), static_cast<const uint8_t*>(W), out, dots, (int)od, (int)K,
-      (int)nt, (int)gemm_ntp(nt), status, limit_ms, stall_ms > 0 ? 1 : 0);
-  return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ELAUNCH;
+      mw, mx, reinterpret_cast<const float2*>(scl), static_cast<const uint8_t*>(W), S > 1 ? part : out, dots,
+      (int)od, (int)K, (int)nt, (int)gemm_ntp(nt), status, limit_ms, stall_ms > 0 ? 1 : 0);
+  if (cudaGetLastError() != cudaSuccess) return QMM_ELAUNCH;
+  if (S > 1) {
+    const int64_t n = nt * od;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    split_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(part, S, n, out);
+    if (cudaGetLastError() != cudaSuccess) return QMM_ELAUNCH;
+  }
+  return QMM_OK;
 }
 
 template <int QT, bool DOTS>
-int launch_qt(const void* W, const __half* xh, const float* scl, float* out, int32_t* dots, int64_t od,
+int launch_qt(const void* W, const __half* xh, const float* scl, float* out, int32_t* dots, float* part, int64_t od,
               int64_t K, int64_t nt, int* status, int stall_ms, cudaStream_t stream) {
   if (DOTS || nt > 64)
-    return launch_cfg<QT, 128, DOTS>(W, xh, scl, out, dots, od, K, nt, status, stall_ms, stream);
-  return launch_cfg<QT, 64, DOTS>(W, xh, scl, out, dots, od, K, nt, status, stall_ms, stream);
+    return launch_cfg<QT, 128, DOTS>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
+  return launch_cfg<QT, 64, DOTS>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
 }
 
 }  // namespace
 
 int launch_gemm_tc(int qtype, const void* W, const __half* xh, const float* scl, float* out, int32_t* dots,
-                   int64_t od, int64_t K, int64_t nt, int* status, int stall_ms, cudaStream_t stream) {
+                   float* part, int64_t od, int64_t K, int64_t nt, int* status, int stall_ms, cudaStream_t stream) {
   if (qtype == QMM_Q4_K)
-    return dots ? launch_qt<kQ4, true>(W, xh, scl, out, dots, od, K, nt, status, stall_ms, stream)
-                : launch_qt<kQ4, false>(W, xh, scl, out, dots, od, K, nt, status, stall_ms, stream);
+    return dots ? launch_qt<kQ4, true>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream)
+                : launch_qt<kQ4, false>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
   if (qtype == QMM_Q6_K) {
     if (K % 2048) return QMM_EINVAL_SHAPE;  // 16-byte row pitch for the TMA weight map
-    return dots ? launch_qt<kQ6, true>(W, xh, scl, out, dots, od, K, nt, status, stall_ms, stream)
-                : launch_qt<kQ6, false>(W, xh, scl, out, dots, od, K, nt, status, stall_ms, stream);
+    return dots ? launch_qt<kQ6, true>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream)
+                : launch_qt<kQ6, false>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
   }
   return QMM_EINVAL_QTYPE;
 }

@@ -21,6 +21,27 @@ inline size_t gemm_xh_bytes(int64_t nt, int64_t K) {
 }
 inline size_t gemm_scl_bytes(int64_t nt, int64_t K) { return (size_t)(K / 32) * gemm_ntp(nt) * 8; }
 
+// Split-K factor of the tensor-core GEMM, a function of the shape alone: a
+// grid of fewer 128-row x token tiles than the 152 SMs of a GB300 takes its K
+// range in up to 8 contiguous slices of whole super-blocks, one slice per
+// CTA, so that about one full wave of CTAs runs.  The slices' fp32 partial
+// sums go to the workspace and are added in a fixed order afterwards.
+inline int gemm_splits(int64_t od, int64_t K, int64_t nt) {
+  const int64_t bn = nt > 64 ? 128 : 64;
+  const int64_t tiles = ((od + 127) / 128) * ((nt + bn - 1) / bn);
+  const int64_t nsb = K / 256;
+  int64_t s = 152 / (tiles > 0 ? tiles : 1);
+  if (s > 8) s = 8;
+  if (s > nsb) s = nsb;
+  if (s < 1) s = 1;
+  const int64_t per = (nsb + s - 1) / s;
+  return (int)((nsb + per - 1) / per);  // every slice is non-empty
+}
+inline size_t gemm_part_bytes(int64_t od, int64_t K, int64_t nt) {
+  const int s = gemm_splits(od, K, nt);
+  return s > 1 ? (size_t)s * (size_t)nt * (size_t)od * sizeof(float) : 0;
+}
+
 // Launch `kern` on `stream`; with `pdl` as a programmatic dependent of the
 // preceding kernel: it may start while that kernel drains and must call
 // griddepcontrol.wait before touching memory the preceding kernel writes.
@@ -64,8 +85,10 @@ int launch_gemv_fused(int qtype, const void* W, const float* x, int8_t* xq, floa
                       int64_t K, int64_t nt, int* status, bool static_w, cudaStream_t stream);
 
 // Tensor-core GEMM over the prepared workspace.  dots != nullptr selects the
-// raw block-dot output (no scale folded into the weight operand).
+// raw block-dot output (no scale folded into the weight operand).  `part`
+// holds gemm_part_bytes of split-K partial sums (unused when the shape does
+// not split).
 int launch_gemm_tc(int qtype, const void* W, const __half* xh, const float* scl, float* out, int32_t* dots,
-                   int64_t od, int64_t K, int64_t nt, int* status, int stall_ms, cudaStream_t stream);
+                   float* part, int64_t od, int64_t K, int64_t nt, int* status, int stall_ms, cudaStream_t stream);
 
 }  // namespace qmm
