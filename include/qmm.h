@@ -181,9 +181,11 @@ int qmm_gemm_builtin_workspace(int qtype, const void *W, const int8_t *xq, const
 /*
  * The whole method from f32 activations, all on `stream` ([CH04] sec. 3.3:
  * the small-batch / prefill split by nt):
- *   - Q4_K with nt*K small enough (nt <= 4, nt*round_up(K, 2048) <= 16384,
- *     the decode shapes): one fused kernel quantizes x to q8_1 inside the
- *     MMVQ kernel (bit-identical codes) and writes xq / xds and out;
+ *   - Q4_K with nt <= 8 whose activations (nt*round_up(K, 2048) codes plus
+ *     the scales) leave room for three 18 KB weight stages in half of an SM's
+ *     shared memory -- about nt*K <= 32768 (the decode and small-batch
+ *     shapes): one fused kernel quantizes x to q8_1 inside the MMVQ kernel
+ *     (bit-identical codes) and writes xq / xds and out;
  *   - other Q4_K with nt <= 8: qmm_quantize_q8_1 into xq / xds, then qmm_gemv;
  *   - otherwise: qmm_quantize_q8_1 (which also writes the GEMM workspace),
  *     then the tensor-core GEMM of qmm_gemm.

@@ -45,8 +45,12 @@ namespace {
 constexpr int kSegSB = 8;                      // super-blocks per stage (2048 k)
 constexpr int kSegBytes = kSegSB * kQ4KBytes;  // 1152 B of one row per stage
 constexpr int kSmemBudget = 200 * 1024;        // staged path (large nt*K)
-constexpr int kFusedRing = 96 * 1024;          // fused path: two CTAs of consecutive kernels fit an SM
-constexpr int64_t kFusedMaxAct = 16384;        // fused path when nt*K <= this
+// Fused path: two CTAs (of consecutive kernels) share an SM, so each gets at
+// most half of the 228 KB less the 1 KB the hardware reserves per CTA; the
+// activations come first and the weight ring takes what is left, 3..5 stages.
+constexpr int kFusedCtaSmem = (228 * 1024 - 2 * 1024) / 2;
+constexpr int kFusedMaxStages = 5;
+constexpr int kFusedMinStages = 3;
 
 template <int NW, int R>
 struct GemvCfg {
@@ -60,6 +64,15 @@ int64_t act_bytes_of(int64_t nt, int64_t K) { return nt * K + nt * (K / 32) * 8;
 // The fused path pads each token's code plane to whole 2048-code stages.
 int64_t fused_plane(int64_t K) { return (K + 2047) / 2048 * 2048; }
 int64_t fused_act_bytes(int64_t nt, int64_t K) { return nt * fused_plane(K) + nt * (K / 32) * 8; }
+
+// Ring stages of the fused kernel for nt x K (16-row, 2048-k stages), 0 if
+// fewer than kFusedMinStages fit next to the activations.
+int fused_stages(int64_t nt, int64_t K) {
+  const int64_t fixed = ((fused_act_bytes(nt, K) + 15) & ~15) + 32 + 1024;
+  int64_t st = (kFusedCtaSmem - fixed) / (16 * kSegBytes + 16);
+  if (st > kFusedMaxStages) st = kFusedMaxStages;
+  return st >= kFusedMinStages ? (int)st : 0;
+}
 
 int stages_for(int64_t nt, int64_t K, int CR, int64_t budget) {
   int s = (int)((budget - act_bytes_of(nt, K) - 1024 - 256) / ((int64_t)CR * kSegBytes));
@@ -472,13 +485,12 @@ int launch_staged(const GemvArgs& a) {
 }
 
 // Fused path: 8 consumer warps of two rows (a 16-row, 18 KB stage) and a
-// ring of about 96 KB, so that a CTA of the next kernel fits on the SM next
-// to this one.
+// ring of 3..5 stages next to the activations, so that a CTA of the next
+// kernel fits on the SM next to this one.
 template <int NT>
 int launch_fused(const GemvArgs& a) {
-  int st = (int)(kFusedRing / (16 * kSegBytes));
-  if (st > 8) st = 8;
-  if (st < 2) return QMM_ESMEM;
+  const int st = fused_stages(NT, a.K);
+  if (st == 0) return QMM_ESMEM;
   return launch_stream<NT, 8, 2, false, true>(a, st);
 }
 
@@ -502,7 +514,7 @@ int launch_q4k_staged(const GemvArgs& a, int64_t nt) {
 bool gemv_fits(int64_t nt, int64_t K) { return nt >= 1 && nt <= 8 && stages_for(nt, K, 8, kSmemBudget) >= 2; }
 
 bool gemv_fused_fits(int64_t nt, int64_t K) {
-  return nt >= 1 && nt <= 4 && nt * fused_plane(K) <= kFusedMaxAct;
+  return nt >= 1 && nt <= 8 && fused_stages(nt, K) > 0;
 }
 
 int launch_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
@@ -526,6 +538,10 @@ int launch_gemv_fused(int qtype, const void* W, const float* x, int8_t* xq, floa
     case 2: return launch_fused<2>(a);
     case 3: return launch_fused<3>(a);
     case 4: return launch_fused<4>(a);
+    case 5: return launch_fused<5>(a);
+    case 6: return launch_fused<6>(a);
+    case 7: return launch_fused<7>(a);
+    case 8: return launch_fused<8>(a);
     default: return QMM_EINVAL_SHAPE;
   }
 }

@@ -71,14 +71,18 @@ def test_strerror_covers_codes():
 
 
 def test_matmul_route_query():
-    """qmm_matmul_path names the route the dispatch takes: the fused decode
-    kernel for small nt*K, quantize + MMVQ up to nt = 8, the tensor-core GEMM
-    beyond (and for Q6_K); workspace is needed exactly on the GEMM route."""
+    """qmm_matmul_path names the route the dispatch takes: the fused
+    quantize + MMVQ kernel for nt <= 8 while the activations leave room for
+    its weight ring (about nt*K <= 32768), quantize + MMVQ for the other
+    nt <= 8, the tensor-core GEMM beyond (and for Q6_K); workspace is needed
+    exactly on the GEMM route."""
     Q4, Q6 = qmm.Q4_K, qmm.Q6_K
     cases = [((Q4, 4096, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 11008, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ),
              ((Q4, 256, 512, 4), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 4096, 4096, 4), qmm.QMM_PATH_FUSED_MMVQ),
-             ((Q4, 4096, 4096, 5), qmm.QMM_PATH_MMVQ), ((Q4, 4096, 4096, 8), qmm.QMM_PATH_MMVQ),
-             ((Q4, 4096, 14336, 2), qmm.QMM_PATH_MMVQ), ((Q4, 4096, 4096, 9), qmm.QMM_PATH_MMQ),
+             ((Q4, 4096, 4096, 5), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 4096, 4096, 8), qmm.QMM_PATH_FUSED_MMVQ),
+             ((Q4, 4096, 14336, 2), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 4096, 14336, 4), qmm.QMM_PATH_MMVQ),
+             ((Q4, 4096, 14336, 8), qmm.QMM_PATH_MMVQ), ((Q4, 14336, 16384, 3), qmm.QMM_PATH_MMVQ),
+             ((Q4, 4096, 4096, 9), qmm.QMM_PATH_MMQ),
              ((Q4, 4096, 4096, 512), qmm.QMM_PATH_MMQ), ((Q6, 4096, 4096, 1), qmm.QMM_PATH_MMQ),
              ((Q6, 32000, 4096, 80), qmm.QMM_PATH_MMQ)]
     for args, path in cases:

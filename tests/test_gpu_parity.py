@@ -172,10 +172,13 @@ def test_workload_skinny_q6k(case):
 
 @pytest.mark.parametrize("od,K,nt,flags", [(4096, 4096, 1, 0), (4096, 4096, 1, 1), (1000, 512, 3, 1),
                                            (300, 768, 4, 0), (11008, 4096, 2, 1), (64, 14336, 1, 1),
-                                           (129, 2304, 2, 0)])
+                                           (129, 2304, 2, 0), (2048, 4096, 8, 1), (1000, 2048, 6, 0),
+                                           (300, 14336, 2, 1), (777, 1280, 7, 0), (4096, 4096, 5, 1)])
 def test_fused_quantize_matmul(od, K, nt, flags):
-    """The fused quantize + MMVQ kernel (decode shapes): q8_1 outputs bit-exact,
-    matmul output within tolerance, with and without the static-weights flag."""
+    """The fused quantize + MMVQ kernel (decode and small-batch shapes): q8_1
+    outputs bit-exact, matmul output within tolerance, with and without the
+    static-weights flag."""
+    assert qmm.qmm_matmul_path(Q4_K, od, K, nt) == qmm.QMM_PATH_FUSED_MMVQ
     W, x = _case(Q4_K, od, K, nt, outliers=True, seed=od + K)
     out, xq, xds = qmm.matmul(Q4_K, dev(W, torch), dev(x, torch), od, flags=flags, return_q8=True)
     oq, ods = ora().quantize_q8_1(x)
