@@ -14,7 +14,8 @@ value   weight GB/s of the whole job: weight bytes of all steps on all ranks /
         CUDA graph of 16 consecutive steps.
 e2e     the same metric with the activations copied from pinned host memory and
         the outputs copied back inside every step, one qmm_matmul call per
-        projection from Python.
+        projection; copy-in, matmuls and copy-out are pipelined on three
+        streams (double-buffered) and replayed from CUDA graphs.
 roofline  the dominant kernel of the step -- the fused quantize + MMVQ kernel of
         the 11008 x 4096 projection -- alone: algorithmic bytes (weights, f32
         activations read, q8_1 activations and f32 outputs written) per launch
@@ -391,31 +392,91 @@ def run_gpu(args):
                 "kernel": kname, "shape": [c.od, c.K], "kernel_us": kernel_ms * 1e3,
                 "alg_bytes_per_launch": alg_bytes, "peak_source": peaks["source"] + " hbm_gbs (copy)"}
 
-    # ---- e2e: host activations in, host outputs back, one C-ABI call per projection
-    xh = [torch.from_numpy(x).pin_memory() for (_, x) in host]
-    oh = [torch.empty((cc.nt, cc.od), dtype=torch.float32).pin_memory() for cc in cases]
-    e2e_steps = max(1, min(args.steps, 2000))
+    # ---- e2e: host activations in, host outputs back, one C-ABI call per
+    # projection.  Every step copies its activations (both projections, one
+    # contiguous buffer) from pinned host memory, runs qmm_matmul for both
+    # projections and copies the outputs back to pinned host memory.  As in a
+    # serving loop the copies are pipelined with compute on their own streams:
+    # activations and outputs are double-buffered on the device, step k's
+    # copy-in overlaps step k-1's matmuls and its copy-out step k+1's.  The
+    # steps are replayed from CUDA graphs of 16 steps.
+    nx = [cc.nt * cc.K for cc in cases]
+    no = [cc.nt * cc.od for cc in cases]
+    x_off = np.cumsum([0] + nx)
+    o_off = np.cumsum([0] + no)
+    xh_all = torch.from_numpy(np.concatenate([x.reshape(-1) for (_, x) in host])).pin_memory()
+    oh_all = [torch.empty(sum(no), dtype=torch.float32).pin_memory() for _ in range(2)]
+    xd_all = [torch.empty(sum(nx), dtype=torch.float32, device=dev) for _ in range(2)]
+    od_all = [torch.empty(sum(no), dtype=torch.float32, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def e2e_capture(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            cs = torch.cuda.current_stream()
+            fork = torch.cuda.Event()
+            fork.record(cs)
+            s_in.wait_event(fork)
+            s_out.wait_event(fork)
+            done, out_done = {}, {}
+            for n, k in enumerate(copies):
+                buf = n % 2
+                if n >= 2:
+                    s_in.wait_event(done[n - 2])  # xd_all[buf] is free again
+                with torch.cuda.stream(s_in):
+                    xd_all[buf].copy_(xh_all, non_blocking=True)
+                x_ready = torch.cuda.Event()
+                x_ready.record(s_in)
+                cs.wait_event(x_ready)
+                if n >= 2:
+                    cs.wait_event(out_done[n - 2])  # od_all[buf] has been copied out
+                for i, cc in enumerate(cases):
+                    rc = qmm.qmm_matmul(cc.qtype, Wcopies[i][k].data_ptr(), xd_all[buf][x_off[i]:].data_ptr(),
+                                        xqs[i].data_ptr(), xdss[i].data_ptr(), od_all[buf][o_off[i]:].data_ptr(),
+                                        cc.od, cc.K, cc.nt, 0, 0, qmm.QMM_FLAG_STATIC_WEIGHTS, cs.cuda_stream)
+                    if rc != qmm.QMM_OK:
+                        raise qmm.QmmError(rc, "qmm_matmul")
+                done[n] = torch.cuda.Event()
+                done[n].record(cs)
+                s_out.wait_event(done[n])
+                with torch.cuda.stream(s_out):
+                    oh_all[buf].copy_(od_all[buf], non_blocking=True)
+                out_done[n] = torch.cuda.Event()
+                out_done[n].record(s_out)
+            join_in, join_out = torch.cuda.Event(), torch.cuda.Event()
+            join_in.record(s_in)
+            join_out.record(s_out)
+            cs.wait_event(join_in)
+            cs.wait_event(join_out)
+        return g
+
+    e_all = e2e_capture(range(NCOPIES))
+    e_one = [e2e_capture([k]) for k in range(NCOPIES)]
+    e2e_steps = max(1, min(args.steps, 16000))
     with torch.cuda.stream(stream):
-        for s in range(e2e_steps + 5):
-            if s == 5:
-                torch.cuda.synchronize()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-            for i, cc in enumerate(cases):
-                xs[i].copy_(xh[i], non_blocking=True)
-                rc = qmm.qmm_matmul(cc.qtype, Wcopies[i][s % NCOPIES].data_ptr(), xs[i].data_ptr(),
-                                    xqs[i].data_ptr(), xdss[i].data_ptr(), outs[i].data_ptr(), cc.od, cc.K,
-                                    cc.nt, 0, 0, qmm.QMM_FLAG_STATIC_WEIGHTS, st)
-                assert rc == qmm.QMM_OK
-                oh[i].copy_(outs[i], non_blocking=True)
+        for _ in range(args.warmup):
+            e_one[0].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps // NCOPIES):
+            e_all.replay()
+        for k in range(e2e_steps % NCOPIES):
+            e_one[k].replay()
         e1.record(stream)
     torch.cuda.synchronize()
+    barrier(world)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    assert qmm.qmm_sync_status(st) == qmm.QMM_OK
+    e2e_ok = all(torch.equal(oh_all[b_], od_all[b_].cpu()) for b_ in range(2))
     e2e = {"value": job_rate(world, wbytes, 1, e2e_ms), "unit": "GB/s",
-           "h2d_bytes_per_step": sum(cc.nt * cc.K * 4 for cc in cases),
-           "d2h_bytes_per_step": sum(cc.nt * cc.od * 4 for cc in cases), "ms_per_step": e2e_ms}
+           "h2d_bytes_per_step": sum(nx) * 4, "d2h_bytes_per_step": sum(no) * 4, "ms_per_step": e2e_ms,
+           "steps": e2e_steps, "outputs_copied_back": bool(e2e_ok),
+           "launch": f"CUDA graphs of {NCOPIES} steps; copy-in, matmuls and copy-out on three streams, "
+                     "double-buffered"}
 
     # ---- CPU baseline: the oracle on this host's cores (rank 0, N = 1 only)
     cpu = None
