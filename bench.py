@@ -379,10 +379,10 @@ def run_gpu(args):
     if route == qmm.QMM_PATH_FUSED_MMVQ:
         # weights + f32 x read + q8_1 written + f32 out written
         alg_bytes = c.weight_bytes + c.nt * c.K * 4 + act_q8 + c.nt * c.od * 4
-        kname = "gemv_q4k_stream_kernel<nt=1, fused> (quantize + MMVQ)"
+        kname = "mmvq_stream_kernel<Q4_K, nt=1, fused> (quantize + MMVQ)"
     else:
         alg_bytes = c.weight_bytes + act_q8 + c.nt * c.od * 4
-        kname = "gemv_q4k_stream_kernel (MMVQ)"
+        kname = "mmvq_stream_kernel (MMVQ)"
     achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
     traffic = (NCU_TRAFFIC["bytes_per_launch"]
                if NCU_TRAFFIC["source_sha1"] == source_sha1("quantized_weight_matmul_gb300/csrc/qmm_gemv.cu")

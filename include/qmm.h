@@ -83,7 +83,7 @@ size_t qmm_xds_bytes(int64_t nt, int64_t K);
  * 0 for invalid input. */
 size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
 
-/* Workspace qmm_matmul needs: 0 on its MMVQ paths (Q4_K, nt <= 8), else
+/* Workspace qmm_matmul needs: 0 on its MMVQ routes (nt <= 8), else
  * qmm_gemm_workspace_bytes. */
 size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
 
@@ -118,11 +118,13 @@ int qmm_quantize_q8_1(const float *x, int64_t nt, int64_t K, int8_t *xq, float *
 
 /*
  * MMVQ: small-batch matmul for 1 <= nt <= 8 ([CH04] sec. 3.4; [MMQ] sec. 12).
- * Streams every weight row once with 16-byte loads and keeps all nt tokens in
- * registers, so the weight traffic does not grow with nt.  Per 32-value
- * sub-block j the integer dot D = sum(nibble * q) is rescaled as
- * d*sc_j*dx*D - dmin*m_j*s.  Q4_K only (QMM_EINVAL_QTYPE for Q6_K, which
- * qmm_matmul sends to the tensor-core path); QMM_ESMEM when the nt x K
+ * Streams every weight row once in TMA-staged tiles and lets every weight
+ * block meet all nt tokens while it is on chip, so the weight traffic does not
+ * grow with nt.  Q4_K: per 32-value sub-block j the integer dot
+ * D = sum(nibble * q) is rescaled as d*sc_j*dx*D - dmin*m_j*s.  Q6_K: per
+ * 16-value group g, D = sum((q6 - 32) * q) is rescaled as d*sc_g*dx*D; Q6_K
+ * needs K % 2048 == 0 (QMM_EINVAL_SHAPE otherwise: the 210-byte blocks give a
+ * 16-byte row pitch only every 8 blocks).  QMM_ESMEM when the nt x K
  * activations do not fit the kernel's shared memory next to its weight ring
  * (nt*K*1.25 bytes above about 180 KB).  out [nt][od] f32 is overwritten.
  */
@@ -181,12 +183,13 @@ int qmm_gemm_builtin_workspace(int qtype, const void *W, const int8_t *xq, const
 /*
  * The whole method from f32 activations, all on `stream` ([CH04] sec. 3.3:
  * the small-batch / prefill split by nt):
- *   - Q4_K with nt <= 8 whose activations (nt*round_up(K, 2048) codes plus
- *     the scales) leave room for three 18 KB weight stages in half of an SM's
- *     shared memory -- about nt*K <= 32768 (the decode and small-batch
- *     shapes): one fused kernel quantizes x to q8_1 inside the MMVQ kernel
- *     (bit-identical codes) and writes xq / xds and out;
- *   - other Q4_K with nt <= 8: qmm_quantize_q8_1 into xq / xds, then qmm_gemv;
+ *   - nt <= 8 whose activations (nt*round_up(K, 2048) codes plus the scales)
+ *     leave room for three weight stages (16 rows x 2048 k: 18 KB for Q4_K,
+ *     26 KB for Q6_K) in half of an SM's shared memory -- about nt*K <= 32768
+ *     for Q4_K (the decode and small-batch shapes): one fused kernel quantizes
+ *     x to q8_1 inside the MMVQ kernel (bit-identical codes) and writes xq /
+ *     xds and out;
+ *   - other nt <= 8: qmm_quantize_q8_1 into xq / xds, then qmm_gemv;
  *   - otherwise: qmm_quantize_q8_1 (which also writes the GEMM workspace),
  *     then the tensor-core GEMM of qmm_gemm.
  * The matmul kernels are launched as programmatic dependents of the kernel
@@ -206,7 +209,7 @@ int qmm_matmul(int qtype, const void *W, const float *x, int8_t *xq, float *xds,
  * as a matmul path but written out before any scaling.
  *   Q4_K: dots[t][r][j] = sum_{i<32} nibble[r][32j+i] * xq[t][32j+i], j < K/32
  *   Q6_K: dots[t][r][g] = sum_{i<16} (q6[r][16g+i] - 32) * xq[t][16g+i], g < K/16
- * path 0: the MMVQ (qmm_gemv) dot code, nt <= 8.
+ * path 0: the MMVQ (qmm_gemv) dot code, nt <= 8 (Q6_K: K % 2048 == 0).
  * path 1: the tensor-core (qmm_gemm) dot code; needs xds (for the prepass)
  *         and a workspace of qmm_gemm_workspace_bytes.
  * dots is a device buffer of nt*od*(K/32 or K/16) int32.

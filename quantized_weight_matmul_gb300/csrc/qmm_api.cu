@@ -68,8 +68,8 @@ size_t gemm_ws(int64_t od, int64_t K, int64_t nt) {
 // The qmm_matmul route for a valid problem (one place, so the query below and
 // the dispatch cannot disagree).
 int matmul_route(int qtype, int64_t nt, int64_t K) {
-  if (qtype == QMM_Q4_K && gemv_fused_fits(nt, K)) return QMM_PATH_FUSED_MMVQ;
-  if (qtype == QMM_Q4_K && nt <= 8 && gemv_fits(nt, K)) return QMM_PATH_MMVQ;
+  if (gemv_fused_fits(qtype, nt, K)) return QMM_PATH_FUSED_MMVQ;
+  if (nt <= 8 && gemv_fits(qtype, nt, K)) return QMM_PATH_MMVQ;
   return QMM_PATH_MMQ;
 }
 
@@ -144,11 +144,11 @@ int qmm_quantize_q8_1(const float* x, int64_t nt, int64_t K, int8_t* xq, float* 
 int qmm_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int64_t od, int64_t K,
              int64_t nt, void* stream) {
   if (!valid_qtype(qtype)) return QMM_EINVAL_QTYPE;
-  if (qtype != QMM_Q4_K) return QMM_EINVAL_QTYPE;  // the MMVQ kernel covers Q4_K
   if (!W || !xq || !xds || !out) return QMM_ENULL;
   int rc = check_shape(od, K, nt);
   if (rc) return rc;
   if (nt > 8) return QMM_EINVAL_SHAPE;
+  if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;  // 16-byte TMA row pitch
   if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
   rc = check_device();
   if (rc) return rc;
@@ -222,8 +222,8 @@ int qmm_debug_block_dots(int qtype, const void* W, const int8_t* xq, const float
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (path == 0) {
-    if (qtype != QMM_Q4_K) return QMM_EINVAL_QTYPE;
     if (nt > 8) return QMM_EINVAL_SHAPE;
+    if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
     if (!xds) return QMM_ENULL;
     int* status = nullptr;
     rc = status_ptr(&status);

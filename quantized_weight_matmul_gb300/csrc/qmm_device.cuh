@@ -205,6 +205,25 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
+// n consecutive 32-bit words starting at byte offset `off` (even) of `base`
+// (4-byte aligned), realigned when off % 4 == 2.
+template <int N>
+__device__ __forceinline__ void load_words_even(const uint8_t* base, int off, uint32_t (&out)[N]) {
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(base + (off & ~3));
+  if (off & 2) {
+    uint32_t prev = p[0];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const uint32_t nxt = p[i + 1];
+      out[i] = prmt(prev, nxt, 0x5432u);
+      prev = nxt;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) out[i] = p[i];
+  }
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -151,25 +151,6 @@ __device__ __forceinline__ void unpack_q4k_pair(const uint8_t* raw_row, int p, u
   }
 }
 
-// n consecutive 32-bit words starting at byte offset `off` (even) of `base`
-// (4-byte aligned), realigned when off % 4 == 2.
-template <int N>
-__device__ __forceinline__ void load_words_even(const uint8_t* base, int off, uint32_t (&out)[N]) {
-  const uint32_t* p = reinterpret_cast<const uint32_t*>(base + (off & ~3));
-  if (off & 2) {
-    uint32_t prev = p[0];
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      const uint32_t nxt = p[i + 1];
-      out[i] = prmt(prev, nxt, 0x5432u);
-      prev = nxt;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < N; ++i) out[i] = p[i];
-  }
-}
-
 // Q6_K: stage s (elements 64s..64s+63 of the super-block) of one row -> 64
 // f16 values q - 32.  Element 128n + 32*quad + l takes its low 4 bits from
 // ql[64n + l] (quads 0, 2) or ql[64n + 32 + l] (quads 1, 3) -- the low nibble

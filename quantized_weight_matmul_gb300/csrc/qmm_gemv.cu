@@ -1,10 +1,14 @@
-// qmm_gemv.cu -- MMVQ: the small-batch (nt <= 8) Q4_K x q8_1 matmul.
+// qmm_gemv.cu -- MMVQ: the small-batch (nt <= 8) Q4_K / Q6_K x q8_1 matmul.
 //
 // What it computes ("04 - Reading minfer's kernels II", sec. 3.4; "llama.cpp
 // MMQ", sec. 12.2; "The quantized GEMM", "The GPU path"): for every weight
 // row r and token t
-//     out[t][r] = sum_j ( d*sc_j*dx_tj*D_trj - dmin*m_j*s_tj ),
-//     D_trj = sum_{i<32} nibble[r][32j+i] * q[t][32j+i]   (exact int32, dp4a)
+//   Q4_K: out[t][r] = sum_j ( d*sc_j*dx_tj*D_trj - dmin*m_j*s_tj ),
+//         D_trj = sum_{i<32} nibble[r][32j+i] * q[t][32j+i]   (exact int32, dp4a)
+//   Q6_K: out[t][r] = sum_g d*sc_g*dx_t(g/2)*D_trg,
+//         D_trg = sum_{i<16} (q6[r][16g+i] - 32) * q[t][16g+i]
+//         (the 6-bit codes are dotted as unsigned bytes; the -32 comes off as
+//         32 x the group's code sum)
 // The weight matrix is streamed from HBM exactly once and every weight block
 // meets all nt tokens while it is on chip: nt never multiplies the weight
 // traffic.
@@ -14,9 +18,9 @@
 // ring of shared-memory stages full with 2-D TMA tiles of the raw weight
 // bytes (CR rows x 8 super-blocks = 2048 k), so tens of KB per SM are in
 // flight whatever the consumers do.  Each consumer warp takes R rows of a
-// stage; lane l handles super-block l/4 of the stage and nibble pair p = l%4,
-// i.e. 64 consecutive weights (sub-blocks 2p and 2p+1), so its activation
-// slice is the same for all R rows.
+// stage; lane l handles super-block l/4 of the stage and part p = l%4 of it,
+// i.e. 64 consecutive weights (Q4_K: sub-blocks 2p and 2p+1; Q6_K: groups
+// 4p..4p+3), so its activation slice is the same for all R rows.
 //
 // Two ways in for the activations:
 //   * staged: q8_1 codes and scales produced by the quantizer are copied
@@ -42,8 +46,10 @@ namespace qmm {
 
 namespace {
 
-constexpr int kSegSB = 8;                      // super-blocks per stage (2048 k)
-constexpr int kSegBytes = kSegSB * kQ4KBytes;  // 1152 B of one row per stage
+constexpr int kQ4 = 0, kQ6 = 1;
+constexpr int kSegSB = 8;  // super-blocks per stage (2048 k)
+// bytes of one row per stage: 1152 (Q4_K), 1680 (Q6_K; a multiple of 16)
+__host__ __device__ constexpr int seg_bytes(int qt) { return kSegSB * (qt == kQ4 ? kQ4KBytes : kQ6KBytes); }
 constexpr int kSmemBudget = 200 * 1024;        // staged path (large nt*K)
 // Fused path: two CTAs (of consecutive kernels) share an SM, so each gets at
 // most half of the 228 KB less the 1 KB the hardware reserves per CTA; the
@@ -52,10 +58,12 @@ constexpr int kFusedCtaSmem = (228 * 1024 - 2 * 1024) / 2;
 constexpr int kFusedMaxStages = 5;
 constexpr int kFusedMinStages = 3;
 
-template <int NW, int R>
+template <int QT, int NW, int R>
 struct GemvCfg {
   static constexpr int CR = NW * R;  // rows per stage (R rows per consumer warp)
-  static constexpr int STAGE_BYTES = CR * kSegBytes;
+  static constexpr int SEG_BYTES = seg_bytes(QT);
+  static constexpr int BLK = QT == kQ4 ? kQ4KBytes : kQ6KBytes;
+  static constexpr int STAGE_BYTES = CR * SEG_BYTES;
   static constexpr int THREADS = 32 * (NW + 1);
 };
 
@@ -67,15 +75,15 @@ int64_t fused_act_bytes(int64_t nt, int64_t K) { return nt * fused_plane(K) + nt
 
 // Ring stages of the fused kernel for nt x K (16-row, 2048-k stages), 0 if
 // fewer than kFusedMinStages fit next to the activations.
-int fused_stages(int64_t nt, int64_t K) {
+int fused_stages(int qt, int64_t nt, int64_t K) {
   const int64_t fixed = ((fused_act_bytes(nt, K) + 15) & ~15) + 32 + 1024;
-  int64_t st = (kFusedCtaSmem - fixed) / (16 * kSegBytes + 16);
+  int64_t st = (kFusedCtaSmem - fixed) / (16 * seg_bytes(qt) + 16);
   if (st > kFusedMaxStages) st = kFusedMaxStages;
   return st >= kFusedMinStages ? (int)st : 0;
 }
 
-int stages_for(int64_t nt, int64_t K, int CR, int64_t budget) {
-  int s = (int)((budget - act_bytes_of(nt, K) - 1024 - 256) / ((int64_t)CR * kSegBytes));
+int stages_for(int qt, int64_t nt, int64_t K, int CR, int64_t budget) {
+  int s = (int)((budget - act_bytes_of(nt, K) - 1024 - 256) / ((int64_t)CR * seg_bytes(qt)));
   return s > 8 ? 8 : s;
 }
 
@@ -112,12 +120,12 @@ __device__ __forceinline__ void named_arrive(int id, int threads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-template <int NT, int NW, int R, bool DOTS, bool FUSED>
+template <int QT, int NT, int NW, int R, bool DOTS, bool FUSED>
 __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
-    gemv_q4k_stream_kernel(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ x,
+    mmvq_stream_kernel(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ x,
                            int8_t* __restrict__ xq, float* __restrict__ xds, float* __restrict__ out,
                            int32_t* __restrict__ dots, int od, int K, int stages, int* status, int static_w) {
-  using C = GemvCfg<NW, R>;
+  using C = GemvCfg<QT, NW, R>;
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t s0 = smem_addr(smem_dyn);
   const uint32_t pad = (1024u - (s0 & 1023u)) & 1023u;
@@ -177,7 +185,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         }
         if (!wait_bar(empty0 + 8 * st, ph ^ 1, g)) break;
         mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE_BYTES);
-        tma_load_2d(sb + st * C::STAGE_BYTES, &tmW, seg * (kSegBytes / 8), grp * C::CR, full0 + 8 * st);
+        tma_load_2d(sb + st * C::STAGE_BYTES, &tmW, seg * (C::SEG_BYTES / 8), grp * C::CR, full0 + 8 * st);
         ++issued;
         if (++st == stages) {
           st = 0;
@@ -293,6 +301,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
       const int kbase = sbi * 256 + 64 * p;
       const int jlo = sbi * 8 + 2 * p;
       const int row0 = grp * C::CR + warp * R;
+      if constexpr (QT == kQ4) {
       // the R weight rows of this lane: nibbles split into the low (sub-block
       // 2p) and high (sub-block 2p+1) planes, and the four scale factors
       const uint8_t* stage = smem + st * C::STAGE_BYTES;
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         const bool use = live && row0 + i < od;
         uint4 hdr = make_uint4(0, 0, 0, 0), q0 = hdr, q1 = hdr;
         if (use) {
-          const uint8_t* blk = stage + (warp * R + i) * kSegBytes + sbo * kQ4KBytes;
+          const uint8_t* blk = stage + (warp * R + i) * C::SEG_BYTES + sbo * kQ4KBytes;
           hdr = *reinterpret_cast<const uint4*>(blk);
           q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * p);
           q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * p);
@@ -368,6 +377,98 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
           }
         }
       }
+      } else {
+      const uint8_t* stage = smem + st * C::STAGE_BYTES;
+      // Q6_K: the lane's 64 values are quads 2(p%2), 2(p%2)+1 of half n = p/2:
+      // low 4 bits from ql[64n + l] / ql[64n + 32 + l] (low nibbles for even p,
+      // high for odd p), top 2 bits from qh[32n + l] (bits 0-1 / 2-3 for even p,
+      // 4-5 / 6-7 for odd p); value q - 32, scale scales[4p + j] per 16 values.
+      // The blocks are 2 bytes aligned: words are read realigned.
+      const int n = p >> 1;
+      const uint32_t shl = (p & 1) ? 4u : 0u, shh = (p & 1) ? 0u : 4u;
+      uint32_t qa[R][8], qb[R][8];
+      float scl[R][4];
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const bool use = live && row0 + i < od;
+        uint32_t L0[8] = {}, L1[8] = {}, H[8] = {}, sw[1] = {0};
+        uint32_t dbits = 0;
+        if (use) {
+          const uint8_t* rowp = stage + (warp * R + i) * C::SEG_BYTES;  // 16-byte aligned
+          const int boff = sbo * kQ6KBytes;                              // even
+          load_words_even<8>(rowp, boff + 64 * n, L0);
+          load_words_even<8>(rowp, boff + 64 * n + 32, L1);
+          load_words_even<8>(rowp, boff + 128 + 32 * n, H);
+          load_words_even<1>(rowp, boff + 192 + 4 * p, sw);
+          dbits = *reinterpret_cast<const uint16_t*>(rowp + boff + 208);
+        }
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const uint32_t h = H[w] << shh;
+          qa[i][w] = ((L0[w] >> shl) & 0x0F0F0F0Fu) | (h & 0x30303030u);
+          qb[i][w] = ((L1[w] >> shl) & 0x0F0F0F0Fu) | ((h >> 2) & 0x30303030u);
+        }
+        const float d = half_bits_to_float(dbits);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) scl[i][j] = d * (float)(int8_t)((sw[0] >> (8 * j)) & 0xFFu);
+      }
+      if (live) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          uint4 x0, x1, x2, x3;
+          if (FUSED) {
+            const uint4* px = reinterpret_cast<const uint4*>(sx + t * Kp) + seg * 128 + lane;
+            x0 = px[0];
+            x1 = px[32];
+            x2 = px[64];
+            x3 = px[96];
+          } else {
+            const uint4* px = reinterpret_cast<const uint4*>(sx + t * K + kbase);
+            x0 = px[0];
+            x1 = px[1];
+            x2 = px[2];
+            x3 = px[3];
+          }
+          const float4 xs = *reinterpret_cast<const float4*>(sds + (t * (K >> 5) + jlo) * 2);
+          const uint32_t xw[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                   x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+          // 32 x the code sum of each 16-value group: the -32 of q - 32
+          int s32[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            int sj = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sj = __dp4a(0x01010101, (int)xw[4 * j + k], sj);
+            s32[j] = 32 * sj;
+          }
+#pragma unroll
+          for (int i = 0; i < R; ++i) {
+            int dj[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              int v = -s32[j];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) v = dp4a_us(j < 2 ? qa[i][4 * j + k] : qb[i][4 * (j - 2) + k], xw[4 * j + k], v);
+              dj[j] = v;  // sum over the group of (q - 32) * x
+            }
+            if constexpr (DOTS) {
+              if (row0 + i < od) {
+                int32_t* dst = dots + ((size_t)t * od + row0 + i) * (K >> 4) + sbi * 16 + 4 * p;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dst[j] = dj[j];
+              }
+            } else {
+              float a = acc[i][t];
+              a = fmaf(scl[i][0] * xs.x, (float)dj[0], a);
+              a = fmaf(scl[i][1] * xs.x, (float)dj[1], a);
+              a = fmaf(scl[i][2] * xs.z, (float)dj[2], a);
+              a = fmaf(scl[i][3] * xs.z, (float)dj[3], a);
+              acc[i][t] = a;
+            }
+          }
+        }
+      }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * st);
       if (!DOTS && seg == nseg - 1) {
@@ -426,15 +527,15 @@ struct GemvArgs {
   cudaStream_t stream;
 };
 
-template <int NT, int NW, int R, bool DOTS, bool FUSED>
+template <int QT, int NT, int NW, int R, bool DOTS, bool FUSED>
 int launch_stream(const GemvArgs& a, int stages) {
-  using C = GemvCfg<NW, R>;
+  using C = GemvCfg<QT, NW, R>;
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QMM_EDEVICE;
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   const int64_t act_bytes = FUSED ? fused_act_bytes(NT, a.K) : act_bytes_of(NT, a.K);
   const int smem = stages * C::STAGE_BYTES + (int)((act_bytes + 15) & ~15) + 16 * stages + 32 + 1024;
-  auto kern = gemv_q4k_stream_kernel<NT, NW, R, DOTS, FUSED>;
+  auto kern = mmvq_stream_kernel<QT, NT, NW, R, DOTS, FUSED>;
   static bool attr_done[64] = {};
   if (dev < 64 && !attr_done[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 8192) !=
@@ -446,11 +547,11 @@ int launch_stream(const GemvArgs& a, int stages) {
   auto fn = gemv_encode_fn();
   if (!fn) return QMM_ELAUNCH;
   // W viewed as [od][row_bytes/8] 8-byte elements; one box = CR rows x 8 super-blocks
-  const uint64_t row_bytes = (uint64_t)(a.K / 256) * kQ4KBytes;
+  const uint64_t row_bytes = (uint64_t)(a.K / 256) * C::BLK;
   CUtensorMap m;
   const cuuint64_t dims[2] = {row_bytes / 8, (cuuint64_t)a.od};
   const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {kSegBytes / 8, (cuuint32_t)C::CR};
+  const cuuint32_t box[2] = {C::SEG_BYTES / 8, (cuuint32_t)C::CR};
   const cuuint32_t estr[2] = {1, 1};
   if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(a.W), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -469,81 +570,99 @@ int launch_stream(const GemvArgs& a, int stages) {
 // (the rows of a warp share its activation registers); fewer rows when the
 // activations leave too little shared memory for a 3-stage ring.  DOTS (a
 // test hook) uses 16 x 1.
-template <int NT, bool DOTS>
+template <int QT, int NT, bool DOTS>
 int launch_staged(const GemvArgs& a) {
   constexpr int NW = (DOTS || NT <= 4) ? 16 : 8;
   constexpr int RP = DOTS ? 1 : (NT <= 2 ? 1 : (NT <= 4 ? 2 : 4));
-  int st = stages_for(NT, a.K, NW * RP, kSmemBudget);
-  if (st >= 3) return launch_stream<NT, NW, RP, DOTS, false>(a, st);
+  int st = stages_for(QT, NT, a.K, NW * RP, kSmemBudget);
+  if (st >= 3) return launch_stream<QT, NT, NW, RP, DOTS, false>(a, st);
   if constexpr (RP >= 2) {
-    st = stages_for(NT, a.K, NW * (RP / 2), kSmemBudget);
-    if (st >= 3) return launch_stream<NT, NW, RP / 2, DOTS, false>(a, st);
+    st = stages_for(QT, NT, a.K, NW * (RP / 2), kSmemBudget);
+    if (st >= 3) return launch_stream<QT, NT, NW, RP / 2, DOTS, false>(a, st);
   }
-  st = stages_for(NT, a.K, 8, kSmemBudget);
-  if (st >= 2) return launch_stream<NT, 8, 1, DOTS, false>(a, st);
+  st = stages_for(QT, NT, a.K, 8, kSmemBudget);
+  if (st >= 2) return launch_stream<QT, NT, 8, 1, DOTS, false>(a, st);
   return QMM_ESMEM;
 }
 
 // Fused path: 8 consumer warps of two rows (a 16-row, 18 KB stage) and a
 // ring of 3..5 stages next to the activations, so that a CTA of the next
 // kernel fits on the SM next to this one.
-template <int NT>
+template <int QT, int NT>
 int launch_fused(const GemvArgs& a) {
-  const int st = fused_stages(NT, a.K);
+  const int st = fused_stages(QT, NT, a.K);
   if (st == 0) return QMM_ESMEM;
-  return launch_stream<NT, 8, 2, false, true>(a, st);
+  return launch_stream<QT, NT, 8, 2, false, true>(a, st);
 }
 
-template <bool DOTS>
-int launch_q4k_staged(const GemvArgs& a, int64_t nt) {
+template <int QT, bool DOTS>
+int launch_staged_nt(const GemvArgs& a, int64_t nt) {
   switch (nt) {
-    case 1: return launch_staged<1, DOTS>(a);
-    case 2: return launch_staged<2, DOTS>(a);
-    case 3: return launch_staged<3, DOTS>(a);
-    case 4: return launch_staged<4, DOTS>(a);
-    case 5: return launch_staged<5, DOTS>(a);
-    case 6: return launch_staged<6, DOTS>(a);
-    case 7: return launch_staged<7, DOTS>(a);
-    case 8: return launch_staged<8, DOTS>(a);
+    case 1: return launch_staged<QT, 1, DOTS>(a);
+    case 2: return launch_staged<QT, 2, DOTS>(a);
+    case 3: return launch_staged<QT, 3, DOTS>(a);
+    case 4: return launch_staged<QT, 4, DOTS>(a);
+    case 5: return launch_staged<QT, 5, DOTS>(a);
+    case 6: return launch_staged<QT, 6, DOTS>(a);
+    case 7: return launch_staged<QT, 7, DOTS>(a);
+    case 8: return launch_staged<QT, 8, DOTS>(a);
     default: return QMM_EINVAL_SHAPE;
   }
+}
+
+template <int QT>
+int launch_fused_nt(const GemvArgs& a, int64_t nt) {
+  switch (nt) {
+    case 1: return launch_fused<QT, 1>(a);
+    case 2: return launch_fused<QT, 2>(a);
+    case 3: return launch_fused<QT, 3>(a);
+    case 4: return launch_fused<QT, 4>(a);
+    case 5: return launch_fused<QT, 5>(a);
+    case 6: return launch_fused<QT, 6>(a);
+    case 7: return launch_fused<QT, 7>(a);
+    case 8: return launch_fused<QT, 8>(a);
+    default: return QMM_EINVAL_SHAPE;
+  }
+}
+
+int qt_of(int qtype) { return qtype == QMM_Q4_K ? kQ4 : kQ6; }
+
+// Q6_K rows are whole 16-byte multiples (a TMA row pitch) only when K is a
+// multiple of 2048 (8 blocks of 210 bytes = 1680).
+bool gemv_type_ok(int qtype, int64_t K) {
+  return qtype == QMM_Q4_K || (qtype == QMM_Q6_K && K % 2048 == 0);
 }
 
 }  // namespace
 
-bool gemv_fits(int64_t nt, int64_t K) { return nt >= 1 && nt <= 8 && stages_for(nt, K, 8, kSmemBudget) >= 2; }
+bool gemv_fits(int qtype, int64_t nt, int64_t K) {
+  return gemv_type_ok(qtype, K) && nt >= 1 && nt <= 8 && stages_for(qt_of(qtype), nt, K, 8, kSmemBudget) >= 2;
+}
 
-bool gemv_fused_fits(int64_t nt, int64_t K) {
-  return nt >= 1 && nt <= 8 && fused_stages(nt, K) > 0;
+bool gemv_fused_fits(int qtype, int64_t nt, int64_t K) {
+  return gemv_type_ok(qtype, K) && nt >= 1 && nt <= 8 && fused_stages(qt_of(qtype), nt, K) > 0;
 }
 
 int launch_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
                 int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream) {
-  if (qtype != QMM_Q4_K) return QMM_EINVAL_QTYPE;
-  if (!gemv_fits(nt, K)) return QMM_ESMEM;
+  if (qtype != QMM_Q4_K && qtype != QMM_Q6_K) return QMM_EINVAL_QTYPE;
+  if (!gemv_type_ok(qtype, K)) return QMM_EINVAL_SHAPE;
+  if (!gemv_fits(qtype, nt, K)) return QMM_ESMEM;
   // right after our quantizer the weight stream may start early: the quantizer
   // releases its dependents only once everything before it has completed
   const GemvArgs a{W,    nullptr, const_cast<int8_t*>(xq), const_cast<float*>(xds), out, dots, od, K, status,
                    after_quantize, after_quantize, stream};
-  return dots ? launch_q4k_staged<true>(a, nt) : launch_q4k_staged<false>(a, nt);
+  if (qtype == QMM_Q4_K)
+    return dots ? launch_staged_nt<kQ4, true>(a, nt) : launch_staged_nt<kQ4, false>(a, nt);
+  return dots ? launch_staged_nt<kQ6, true>(a, nt) : launch_staged_nt<kQ6, false>(a, nt);
 }
 
 int launch_gemv_fused(int qtype, const void* W, const float* x, int8_t* xq, float* xds, float* out, int64_t od,
                       int64_t K, int64_t nt, int* status, bool static_w, cudaStream_t stream) {
-  if (qtype != QMM_Q4_K) return QMM_EINVAL_QTYPE;
-  if (!gemv_fused_fits(nt, K)) return QMM_ESMEM;
+  if (qtype != QMM_Q4_K && qtype != QMM_Q6_K) return QMM_EINVAL_QTYPE;
+  if (!gemv_fused_fits(qtype, nt, K)) return QMM_ESMEM;
   const GemvArgs a{W, x, xq, xds, out, nullptr, od, K, status, true, static_w, stream};
-  switch (nt) {
-    case 1: return launch_fused<1>(a);
-    case 2: return launch_fused<2>(a);
-    case 3: return launch_fused<3>(a);
-    case 4: return launch_fused<4>(a);
-    case 5: return launch_fused<5>(a);
-    case 6: return launch_fused<6>(a);
-    case 7: return launch_fused<7>(a);
-    case 8: return launch_fused<8>(a);
-    default: return QMM_EINVAL_SHAPE;
-  }
+  return qtype == QMM_Q4_K ? launch_fused_nt<kQ4>(a, nt) : launch_fused_nt<kQ6>(a, nt);
 }
 
 }  // namespace qmm

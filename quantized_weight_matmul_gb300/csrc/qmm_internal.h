@@ -66,10 +66,11 @@ int launch_quantize(const float* x, int64_t nt, int64_t K, int8_t* xq, float* xd
 int launch_gemm_prep(const int8_t* xq, const float* xds, int64_t nt, int64_t K, int64_t ntp, __half* xh,
                      float* scl, cudaStream_t stream);
 
-// Whether the MMVQ kernel can stage nt x K activations next to its weight ring.
-bool gemv_fits(int64_t nt, int64_t K);
+// Whether the MMVQ kernel can stage nt x K activations next to its weight ring
+// (Q4_K, or Q6_K with K a multiple of 2048).
+bool gemv_fits(int qtype, int64_t nt, int64_t K);
 // Whether the fused quantize + MMVQ kernel covers nt x K (decode shapes).
-bool gemv_fused_fits(int64_t nt, int64_t K);
+bool gemv_fused_fits(int qtype, int64_t nt, int64_t K);
 
 // MMVQ (nt <= 8).  dots != nullptr selects the raw block-dot output.  With
 // `after_quantize` the kernel is launched as a programmatic dependent of the

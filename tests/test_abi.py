@@ -48,6 +48,7 @@ def test_argument_checks_need_no_device():
     assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 300, 1, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 256, 9, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 0, 256, 1, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_gemv(qmm.Q6_K, p, p, p, p, 256, 1024, 1, 0) == qmm.QMM_EINVAL_SHAPE  # Q6_K: K % 2048
     assert qmm.qmm_gemv(qmm.Q4_K, p + 1, p, p, p, 256, 256, 1, 0) == qmm.QMM_EALIGN
     assert qmm.qmm_quantize_q8_1(p, 1, 48, p, p, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_gemm(qmm.Q4_K, p, p, p, p, 256, 256, 0, p, 4096, 0) == qmm.QMM_EINVAL_SHAPE
@@ -73,9 +74,9 @@ def test_strerror_covers_codes():
 def test_matmul_route_query():
     """qmm_matmul_path names the route the dispatch takes: the fused
     quantize + MMVQ kernel for nt <= 8 while the activations leave room for
-    its weight ring (about nt*K <= 32768), quantize + MMVQ for the other
-    nt <= 8, the tensor-core GEMM beyond (and for Q6_K); workspace is needed
-    exactly on the GEMM route."""
+    its weight ring (about nt*K <= 32768 for Q4_K; smaller for Q6_K's larger
+    stages), quantize + MMVQ for the other nt <= 8, the tensor-core GEMM
+    beyond; workspace is needed exactly on the GEMM route."""
     Q4, Q6 = qmm.Q4_K, qmm.Q6_K
     cases = [((Q4, 4096, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 11008, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ),
              ((Q4, 256, 512, 4), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 4096, 4096, 4), qmm.QMM_PATH_FUSED_MMVQ),
@@ -83,8 +84,9 @@ def test_matmul_route_query():
              ((Q4, 4096, 14336, 2), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 4096, 14336, 4), qmm.QMM_PATH_MMVQ),
              ((Q4, 4096, 14336, 8), qmm.QMM_PATH_MMVQ), ((Q4, 14336, 16384, 3), qmm.QMM_PATH_MMVQ),
              ((Q4, 4096, 4096, 9), qmm.QMM_PATH_MMQ),
-             ((Q4, 4096, 4096, 512), qmm.QMM_PATH_MMQ), ((Q6, 4096, 4096, 1), qmm.QMM_PATH_MMQ),
-             ((Q6, 32000, 4096, 80), qmm.QMM_PATH_MMQ)]
+             ((Q4, 4096, 4096, 512), qmm.QMM_PATH_MMQ), ((Q6, 4096, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ),
+             ((Q6, 32000, 4096, 2), qmm.QMM_PATH_FUSED_MMVQ), ((Q6, 4096, 4096, 8), qmm.QMM_PATH_MMVQ),
+             ((Q6, 4096, 4096, 9), qmm.QMM_PATH_MMQ), ((Q6, 32000, 4096, 80), qmm.QMM_PATH_MMQ)]
     for args, path in cases:
         assert qmm.qmm_matmul_path(*args) == path, args
         assert (qmm.qmm_matmul_workspace_bytes(*args) > 0) == (path == qmm.QMM_PATH_MMQ), args

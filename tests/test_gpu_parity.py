@@ -102,6 +102,17 @@ def test_gemv_block_dots_bit_exact(od, K, nt):
     assert np.array_equal(d.cpu().numpy(), ora().block_dots(Q4_K, W, xq, od))
 
 
+@pytest.mark.parametrize("od,K,nt", [(256, 2048, 1), (300, 4096, 8), (1, 2048, 3), (4096, 4096, 1),
+                                     (130, 6144, 5)])
+def test_gemv_q6k_block_dots_bit_exact(od, K, nt):
+    """Q6_K through the MMVQ dot code: sum over each 16-value group of
+    (q6 - 32) * q8, exact int32."""
+    W, x = _case(Q6_K, od, K, nt, seed=od + 1)
+    xq, xds = ora().quantize_q8_1(x)
+    d = qmm.block_dots(Q6_K, dev(W, torch), dev(xq, torch), dev(xds, torch), od, path=0)
+    assert np.array_equal(d.cpu().numpy(), ora().block_dots(Q6_K, W, xq, od))
+
+
 @pytest.mark.parametrize("qtype,od,K,nt", [(Q4_K, 300, 512, 70), (Q4_K, 129, 1024, 200),
                                            (Q4_K, 128, 256, 1), (Q6_K, 300, 2048, 70),
                                            (Q6_K, 130, 4096, 131)])
@@ -126,6 +137,34 @@ def test_gemv_matches_oracle(od, K, nt):
     out = qmm.gemv(Q4_K, dev(W, torch), dev(xq, torch), dev(xds, torch), od)
     ref = ora().matmul_q8_1(Q4_K, W, xq, xds, od, nthreads=threads())
     assert_close_rows(out.cpu().numpy(), ref, f"gemv {od}x{K} nt={nt}")
+
+
+@pytest.mark.parametrize("od,K,nt", [(256, 2048, 1), (1000, 4096, 5), (4096, 4096, 8), (129, 6144, 2),
+                                     (32000, 4096, 1), (33, 2048, 7)])
+def test_gemv_q6k_matches_oracle(od, K, nt):
+    W, x = _case(Q6_K, od, K, nt, outliers=(nt == 1), seed=2)
+    xq, xds = ora().quantize_q8_1(x)
+    out = qmm.gemv(Q6_K, dev(W, torch), dev(xq, torch), dev(xds, torch), od).cpu().numpy()
+    rows = row_sample(od)
+    ref = oracle_rows(Q6_K, W, x, rows) if od > 4096 else ora().matmul_q8_1(Q6_K, W, xq, xds, od, nthreads=threads())
+    assert_close_rows(out[:, rows] if od > 4096 else out, ref, f"q6k gemv {od}x{K} nt={nt}")
+
+
+@pytest.mark.parametrize("od,K,nt", [(4096, 4096, 1), (300, 2048, 3), (32000, 4096, 2), (1000, 2048, 4)])
+def test_fused_q6k_matmul(od, K, nt):
+    """Q6_K decode shapes take the fused quantize + MMVQ kernel: q8_1 outputs
+    bit-exact, outputs within tolerance."""
+    assert qmm.qmm_matmul_path(Q6_K, od, K, nt) == qmm.QMM_PATH_FUSED_MMVQ
+    W, x = _case(Q6_K, od, K, nt, outliers=True, seed=od)
+    out, xq, xds = qmm.matmul(Q6_K, dev(W, torch), dev(x, torch), od, flags=qmm.QMM_FLAG_STATIC_WEIGHTS,
+                              return_q8=True)
+    oq, ods = ora().quantize_q8_1(x)
+    assert np.array_equal(xq.cpu().numpy(), oq)
+    assert np.array_equal(xds.cpu().numpy().view(np.uint32), ods.view(np.uint32))
+    rows = row_sample(od)
+    ref = oracle_rows(Q6_K, W, x, rows)
+    assert_close_rows(out.cpu().numpy()[:, rows], ref, f"fused q6k {od}x{K} nt={nt}")
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
 
 
 # ---------------------------------------------------------------- GEMM ---
