@@ -539,7 +539,7 @@ def run_sweep(args):
             xq, xds = qmm.quantize_q8_1(xd)
             out = torch.empty((c.nt, c.od), dtype=torch.float32, device=dev)
             route = qmm.qmm_matmul_path(c.qtype, c.od, c.K, c.nt)
-            use_gemv = c.qtype == qmm.Q4_K and c.nt <= 8 and route != qmm.QMM_PATH_MMQ
+            use_gemv = c.nt <= qmm.qmm_gemv_max_nt() and route != qmm.QMM_PATH_MMQ
             need = qmm.qmm_gemm_workspace_bytes(c.qtype, c.od, c.K, c.nt)
             ws = qmm.workspace(need, dev)
             xq8 = torch.empty((c.nt, c.K), dtype=torch.int8, device=dev)

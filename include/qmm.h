@@ -30,7 +30,7 @@
  *     16-byte aligned base); x and xq are token-major [nt][K]; xds is
  *     [nt][K/32][2] f32 = (d, s); out is [nt][od] f32, od contiguous.
  *   - Preconditions checked on the host: qtype is QMM_Q4_K or QMM_Q6_K;
- *     K > 0 and K % 256 == 0; od >= 1; nt >= 1 (qmm_gemv: 1 <= nt <= 8);
+ *     K > 0 and K % 256 == 0; od >= 1; nt >= 1 (qmm_gemv: 1 <= nt <= 16);
  *     od, K, nt and od*nt, nt*K below 2^31; non-NULL pointers; W, x, xq,
  *     xds, out and the workspace 16-byte aligned.  Inputs must be finite.
  *   - Every call returns QMM_OK (0) or a negative QMM_E* code and launches
@@ -97,7 +97,7 @@ size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
  * only; it depends on nothing but its arguments. */
 int qmm_matmul_path(int qtype, int64_t od, int64_t K, int64_t nt);
 
-/* Largest nt qmm_gemv accepts (8, the register token loop of [MMQ] sec. 12). */
+/* Largest nt qmm_gemv accepts (16: two 8-token tiles of the warp-MMA MMVQ). */
 int qmm_gemv_max_nt(void);
 
 /* ------------------------------------------------------- device work ---- */
@@ -117,16 +117,19 @@ int qmm_quantize_q8_1(const float *x, int64_t nt, int64_t K, int8_t *xq, float *
                       void *stream);
 
 /*
- * MMVQ: small-batch matmul for 1 <= nt <= 8 ([CH04] sec. 3.4; [MMQ] sec. 12).
+ * MMVQ: small-batch matmul for 1 <= nt <= 16 ([CH04] sec. 3.4; [MMQ] sec. 12).
  * Streams every weight row once in TMA-staged tiles and lets every weight
  * block meet all nt tokens while it is on chip, so the weight traffic does not
  * grow with nt.  Q4_K: per 32-value sub-block j the integer dot
  * D = sum(nibble * q) is rescaled as d*sc_j*dx*D - dmin*m_j*s.  Q6_K: per
  * 16-value group g, D = sum((q6 - 32) * q) is rescaled as d*sc_g*dx*D; Q6_K
  * needs K % 2048 == 0 (QMM_EINVAL_SHAPE otherwise: the 210-byte blocks give a
- * 16-byte row pitch only every 8 blocks).  QMM_ESMEM when the nt x K
- * activations do not fit the kernel's shared memory next to its weight ring
- * (nt*K*1.25 bytes above about 180 KB).  out [nt][od] f32 is overwritten.
+ * 16-byte row pitch only every 8 blocks).  Few tokens (nt <= 4 for Q4_K,
+ * nt = 1 for Q6_K) take the dp4a kernel, more tokens the warp-level
+ * tensor-core MMA kernel (mma.sync on exact small-integer f16 operands).
+ * QMM_ESMEM when the nt x K activations do not fit the chosen kernel's shared
+ * memory next to its weight ring (for nt > 8 only the MMA kernel applies:
+ * about nt*K <= 96K codes).  out [nt][od] f32 is overwritten.
  */
 int qmm_gemv(int qtype, const void *W, const int8_t *xq, const float *xds, float *out,
              int64_t od, int64_t K, int64_t nt, void *stream);
@@ -183,12 +186,14 @@ int qmm_gemm_builtin_workspace(int qtype, const void *W, const int8_t *xq, const
 /*
  * The whole method from f32 activations, all on `stream` ([CH04] sec. 3.3:
  * the small-batch / prefill split by nt):
- *   - nt <= 8 whose activations (nt*round_up(K, 2048) codes plus the scales)
- *     leave room for three weight stages (16 rows x 2048 k: 18 KB for Q4_K,
- *     26 KB for Q6_K) in half of an SM's shared memory -- about nt*K <= 32768
- *     for Q4_K (the decode and small-batch shapes): one fused kernel quantizes
- *     x to q8_1 inside the MMVQ kernel (bit-identical codes) and writes xq /
- *     xds and out;
+ *   - from 5 tokens (Q4_K) or 2 (Q6_K) up to 16, where the activations fit
+ *     the warp-MMA MMVQ's shared memory: qmm_quantize_q8_1 into xq / xds,
+ *     then qmm_gemv on the MMA kernel;
+ *   - other nt <= 8 whose activations (nt*round_up(K, 2048) codes plus the
+ *     scales) leave room for three weight stages (16 rows x 2048 k: 18 KB for
+ *     Q4_K, 26 KB for Q6_K) in half of an SM's shared memory (the decode
+ *     shapes): one fused kernel quantizes x to q8_1 inside the dp4a MMVQ
+ *     kernel (bit-identical codes) and writes xq / xds and out;
  *   - other nt <= 8: qmm_quantize_q8_1 into xq / xds, then qmm_gemv;
  *   - otherwise: qmm_quantize_q8_1 (which also writes the GEMM workspace),
  *     then the tensor-core GEMM of qmm_gemm.
@@ -209,9 +214,11 @@ int qmm_matmul(int qtype, const void *W, const float *x, int8_t *xq, float *xds,
  * as a matmul path but written out before any scaling.
  *   Q4_K: dots[t][r][j] = sum_{i<32} nibble[r][32j+i] * xq[t][32j+i], j < K/32
  *   Q6_K: dots[t][r][g] = sum_{i<16} (q6[r][16g+i] - 32) * xq[t][16g+i], g < K/16
- * path 0: the MMVQ (qmm_gemv) dot code, nt <= 8 (Q6_K: K % 2048 == 0).
+ * path 0: the dp4a MMVQ dot code, nt <= 8 (Q6_K: K % 2048 == 0).
  * path 1: the tensor-core (qmm_gemm) dot code; needs xds (for the prepass)
  *         and a workspace of qmm_gemm_workspace_bytes.
+ * path 2: the warp-MMA MMVQ dot code, nt <= 16 (Q6_K: K % 2048 == 0); needs
+ *         xds; QMM_ESMEM where the activations do not fit its shared memory.
  * dots is a device buffer of nt*od*(K/32 or K/16) int32.
  */
 int qmm_debug_block_dots(int qtype, const void *W, const int8_t *xq, const float *xds,

@@ -68,6 +68,7 @@ size_t gemm_ws(int64_t od, int64_t K, int64_t nt) {
 // The qmm_matmul route for a valid problem (one place, so the query below and
 // the dispatch cannot disagree).
 int matmul_route(int qtype, int64_t nt, int64_t K) {
+  if (nt >= mma_min_nt(qtype) && mmvq_mma_fits(qtype, nt, K)) return QMM_PATH_MMVQ;
   if (gemv_fused_fits(qtype, nt, K)) return QMM_PATH_FUSED_MMVQ;
   if (nt <= 8 && gemv_fits(qtype, nt, K)) return QMM_PATH_MMVQ;
   return QMM_PATH_MMQ;
@@ -130,7 +131,7 @@ int qmm_matmul_path(int qtype, int64_t od, int64_t K, int64_t nt) {
   return path;
 }
 
-int qmm_gemv_max_nt(void) { return 8; }
+int qmm_gemv_max_nt(void) { return kMmaMaxNt; }
 
 int qmm_quantize_q8_1(const float* x, int64_t nt, int64_t K, int8_t* xq, float* xds, void* stream) {
   if (!x || !xq || !xds) return QMM_ENULL;
@@ -147,7 +148,7 @@ int qmm_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float
   if (!W || !xq || !xds || !out) return QMM_ENULL;
   int rc = check_shape(od, K, nt);
   if (rc) return rc;
-  if (nt > 8) return QMM_EINVAL_SHAPE;
+  if (nt > kMmaMaxNt) return QMM_EINVAL_SHAPE;
   if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;  // 16-byte TMA row pitch
   if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
   rc = check_device();
@@ -229,6 +230,16 @@ int qmm_debug_block_dots(int qtype, const void* W, const int8_t* xq, const float
     rc = status_ptr(&status);
     if (rc) return rc;
     return launch_gemv(qtype, W, xq, xds, nullptr, dots, od, K, nt, status, false, st);
+  }
+  if (path == 2) {
+    if (nt > kMmaMaxNt) return QMM_EINVAL_SHAPE;
+    if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
+    if (!xds) return QMM_ENULL;
+    if (!aligned16(xds)) return QMM_EALIGN;
+    int* status = nullptr;
+    rc = status_ptr(&status);
+    if (rc) return rc;
+    return launch_mmvq_mma(qtype, W, xq, xds, nullptr, dots, od, K, nt, status, false, st);
   }
   if (path != 1) return QMM_EINVAL_SHAPE;
   if (!xds) return QMM_ENULL;

@@ -55,6 +55,22 @@ __device__ __forceinline__ void q4k_scale_min_words(uint32_t w0, uint32_t w1, ui
   }
 }
 
+// The (scale, min) pairs of sub-blocks 2p and 2p+1 from the header
+// words holding scales[0..11] ("llama.cpp MMQ", sec. 6): sub-blocks 0-3 keep
+// both 6-bit codes in bytes j and j+4; sub-blocks 4-7 keep the low 4 bits in
+// the nibbles of byte j+4 and the top 2 bits in the top of bytes j-4 / j.
+// Returns the two codes of each kind in the low two bytes.
+__device__ __forceinline__ void q4k_pair_codes(uint32_t w1, uint32_t w2, uint32_t w3, int p, uint32_t& sc2,
+                                               uint32_t& m2) {
+  const uint32_t sh = 16u * (p & 1);
+  const uint32_t t1 = (w1 >> sh) & 0xFFFFu, t2 = (w2 >> sh) & 0xFFFFu, t3 = (w3 >> sh) & 0xFFFFu;
+  const uint32_t sc_low = t1 & 0x3F3Fu, m_low = t2 & 0x3F3Fu;
+  const uint32_t sc_high = (t3 & 0x0F0Fu) | ((t1 >> 2) & 0x3030u);
+  const uint32_t m_high = ((t3 >> 4) & 0x0F0Fu) | ((t2 >> 2) & 0x3030u);
+  sc2 = p < 2 ? sc_low : sc_high;
+  m2 = p < 2 ? m_low : m_high;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

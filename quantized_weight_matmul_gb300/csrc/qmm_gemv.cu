@@ -87,22 +87,6 @@ int stages_for(int qt, int64_t nt, int64_t K, int CR, int64_t budget) {
   return s > 8 ? 8 : s;
 }
 
-// Decode the (scale, min) pairs of sub-blocks 2p and 2p+1 from the header
-// words holding scales[0..11] ("llama.cpp MMQ", sec. 6): sub-blocks 0-3 keep
-// both 6-bit codes in bytes j and j+4; sub-blocks 4-7 keep the low 4 bits in
-// the nibbles of byte j+4 and the top 2 bits in the top of bytes j-4 / j.
-// Returns the two codes of each kind in the low two bytes.
-__device__ __forceinline__ void q4k_pair_codes(uint32_t w1, uint32_t w2, uint32_t w3, int p, uint32_t& sc2,
-                                               uint32_t& m2) {
-  const uint32_t sh = 16u * (p & 1);
-  const uint32_t t1 = (w1 >> sh) & 0xFFFFu, t2 = (w2 >> sh) & 0xFFFFu, t3 = (w3 >> sh) & 0xFFFFu;
-  const uint32_t sc_low = t1 & 0x3F3Fu, m_low = t2 & 0x3F3Fu;
-  const uint32_t sc_high = (t3 & 0x0F0Fu) | ((t1 >> 2) & 0x3030u);
-  const uint32_t m_high = ((t3 >> 4) & 0x0F0Fu) | ((t2 >> 2) & 0x3030u);
-  sc2 = p < 2 ? sc_low : sc_high;
-  m2 = p < 2 ? m_low : m_high;
-}
-
 // Byte offset, in the fused path's shared activation plane of one token, of
 // code k: the 64 codes a lane reads per stage are split into four 16-byte
 // chunks stored chunk-major across the 32 lanes, so a warp's chunk loads
@@ -501,19 +485,6 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
   __syncthreads();
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 gemv_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
 struct GemvArgs {
   const void* W;
   const float* x;  // fused path
@@ -544,7 +515,7 @@ int launch_stream(const GemvArgs& a, int stages) {
     attr_done[dev] = true;
   }
   if (smem > kSmemBudget + 8192) return QMM_ESMEM;
-  auto fn = gemv_encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return QMM_ELAUNCH;
   // W viewed as [od][row_bytes/8] 8-byte elements; one box = CR rows x 8 super-blocks
   const uint64_t row_bytes = (uint64_t)(a.K / 256) * C::BLK;
@@ -610,6 +581,7 @@ int launch_staged_nt(const GemvArgs& a, int64_t nt) {
   }
 }
 
+// (from 5 tokens qmm_matmul takes the warp-MMA kernel instead)
 template <int QT>
 int launch_fused_nt(const GemvArgs& a, int64_t nt) {
   switch (nt) {
@@ -617,10 +589,6 @@ int launch_fused_nt(const GemvArgs& a, int64_t nt) {
     case 2: return launch_fused<QT, 2>(a);
     case 3: return launch_fused<QT, 3>(a);
     case 4: return launch_fused<QT, 4>(a);
-    case 5: return launch_fused<QT, 5>(a);
-    case 6: return launch_fused<QT, 6>(a);
-    case 7: return launch_fused<QT, 7>(a);
-    case 8: return launch_fused<QT, 8>(a);
     default: return QMM_EINVAL_SHAPE;
   }
 }
@@ -635,18 +603,34 @@ bool gemv_type_ok(int qtype, int64_t K) {
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
 bool gemv_fits(int qtype, int64_t nt, int64_t K) {
   return gemv_type_ok(qtype, K) && nt >= 1 && nt <= 8 && stages_for(qt_of(qtype), nt, K, 8, kSmemBudget) >= 2;
 }
 
 bool gemv_fused_fits(int qtype, int64_t nt, int64_t K) {
-  return gemv_type_ok(qtype, K) && nt >= 1 && nt <= 8 && fused_stages(qt_of(qtype), nt, K) > 0;
+  return gemv_type_ok(qtype, K) && nt >= 1 && nt <= 4 && fused_stages(qt_of(qtype), nt, K) > 0;
 }
 
 int launch_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
                 int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream) {
   if (qtype != QMM_Q4_K && qtype != QMM_Q6_K) return QMM_EINVAL_QTYPE;
   if (!gemv_type_ok(qtype, K)) return QMM_EINVAL_SHAPE;
+  // from a few tokens on the dots run on the warp-level tensor-core MMA
+  if (!dots && (nt > 8 || nt >= mma_min_nt(qtype)) && mmvq_mma_fits(qtype, nt, K))
+    return launch_mmvq_mma(qtype, W, xq, xds, out, nullptr, od, K, nt, status, after_quantize, stream);
   if (!gemv_fits(qtype, nt, K)) return QMM_ESMEM;
   // right after our quantizer the weight stream may start early: the quantizer
   // releases its dependents only once everything before it has completed

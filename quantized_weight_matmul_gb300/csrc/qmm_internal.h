@@ -4,8 +4,10 @@
 #include <cstddef>
 #include <cstdint>
 #include <utility>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "qmm.h"
 
@@ -61,6 +63,9 @@ int launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaSt
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) == cudaSuccess ? QMM_OK : QMM_ELAUNCH;
 }
 
+// The driver's cuTensorMapEncodeTiled, looked up once (nullptr if absent).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 int launch_quantize(const float* x, int64_t nt, int64_t K, int8_t* xq, float* xds, __half* xh,
                     float* scl, int64_t ntp, cudaStream_t stream);
 int launch_gemm_prep(const int8_t* xq, const float* xds, int64_t nt, int64_t K, int64_t ntp, __half* xh,
@@ -69,7 +74,7 @@ int launch_gemm_prep(const int8_t* xq, const float* xds, int64_t nt, int64_t K, 
 // Whether the MMVQ kernel can stage nt x K activations next to its weight ring
 // (Q4_K, or Q6_K with K a multiple of 2048).
 bool gemv_fits(int qtype, int64_t nt, int64_t K);
-// Whether the fused quantize + MMVQ kernel covers nt x K (decode shapes).
+// Whether the fused quantize + MMVQ kernel covers nt x K (decode shapes, nt <= 4).
 bool gemv_fused_fits(int qtype, int64_t nt, int64_t K);
 
 // MMVQ (nt <= 8).  dots != nullptr selects the raw block-dot output.  With
@@ -79,6 +84,18 @@ bool gemv_fused_fits(int qtype, int64_t nt, int64_t K);
 // are ready.
 int launch_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
                 int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream);
+
+// Warp-MMA MMVQ (qmm_mmvq_mma.cu) for 1 <= nt <= kMmaMaxNt: whether the
+// activations and a weight ring of at least two stages fit one SM's shared
+// memory (Q6_K also needs K % 2048 == 0), and the launcher.  dots != nullptr
+// selects the raw block-dot output; `after_quantize` as for launch_gemv.
+constexpr int kMmaMaxNt = 16;
+// Smallest nt the warp-MMA kernel takes (below it the dp4a MMVQ is faster:
+// its cost per token is small while the MMA's 8-token tile is mostly padding).
+inline int mma_min_nt(int qtype) { return qtype == QMM_Q4_K ? 5 : 2; }
+bool mmvq_mma_fits(int qtype, int64_t nt, int64_t K);
+int launch_mmvq_mma(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
+                    int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream);
 
 // Fused quantize + MMVQ: x f32 in, q8_1 (xq, xds) and out written.  With
 // `static_w` the weight stream starts before the preceding kernel completes.

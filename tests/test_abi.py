@@ -31,7 +31,7 @@ def test_weight_and_activation_sizes():
     assert qmm.qmm_weight_bytes(7, 16, 256) == 0
     assert qmm.qmm_xq_bytes(3, 512) == 1536
     assert qmm.qmm_xds_bytes(3, 512) == 3 * 16 * 8
-    assert qmm.qmm_gemv_max_nt() == 8
+    assert qmm.qmm_gemv_max_nt() == 16
     assert qmm.qmm_matmul_workspace_bytes(qmm.Q4_K, 4096, 4096, 8) == 0
     ws = qmm.qmm_gemm_workspace_bytes(qmm.Q4_K, 4096, 4096, 512)
     assert ws >= 512 * 4096 * 2 + 4096 // 32 * 512 * 8
@@ -46,7 +46,7 @@ def test_argument_checks_need_no_device():
     assert qmm.qmm_gemv(5, p, p, p, p, 256, 256, 1, 0) == qmm.QMM_EINVAL_QTYPE
     assert qmm.qmm_gemv(qmm.Q4_K, 0, p, p, p, 256, 256, 1, 0) == qmm.QMM_ENULL
     assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 300, 1, 0) == qmm.QMM_EINVAL_SHAPE
-    assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 256, 9, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 256, 17, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 0, 256, 1, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_gemv(qmm.Q6_K, p, p, p, p, 256, 1024, 1, 0) == qmm.QMM_EINVAL_SHAPE  # Q6_K: K % 2048
     assert qmm.qmm_gemv(qmm.Q4_K, p + 1, p, p, p, 256, 256, 1, 0) == qmm.QMM_EALIGN
@@ -73,20 +73,20 @@ def test_strerror_covers_codes():
 
 def test_matmul_route_query():
     """qmm_matmul_path names the route the dispatch takes: the fused
-    quantize + MMVQ kernel for nt <= 8 while the activations leave room for
-    its weight ring (about nt*K <= 32768 for Q4_K; smaller for Q6_K's larger
-    stages), quantize + MMVQ for the other nt <= 8, the tensor-core GEMM
+    quantize + dp4a MMVQ kernel for few tokens (nt = 1, and Q4_K up to 4)
+    while the activations leave room for its weight ring, quantize + the
+    warp-MMA MMVQ from 5 tokens (Q4_K) or 2 (Q6_K) up to 16 where it fits,
+    quantize + the dp4a MMVQ for the other nt <= 8, the tensor-core GEMM
     beyond; workspace is needed exactly on the GEMM route."""
     Q4, Q6 = qmm.Q4_K, qmm.Q6_K
-    cases = [((Q4, 4096, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 11008, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ),
-             ((Q4, 256, 512, 4), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 4096, 4096, 4), qmm.QMM_PATH_FUSED_MMVQ),
-             ((Q4, 4096, 4096, 5), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 4096, 4096, 8), qmm.QMM_PATH_FUSED_MMVQ),
-             ((Q4, 4096, 14336, 2), qmm.QMM_PATH_FUSED_MMVQ), ((Q4, 4096, 14336, 4), qmm.QMM_PATH_MMVQ),
-             ((Q4, 4096, 14336, 8), qmm.QMM_PATH_MMVQ), ((Q4, 14336, 16384, 3), qmm.QMM_PATH_MMVQ),
-             ((Q4, 4096, 4096, 9), qmm.QMM_PATH_MMQ),
-             ((Q4, 4096, 4096, 512), qmm.QMM_PATH_MMQ), ((Q6, 4096, 4096, 1), qmm.QMM_PATH_FUSED_MMVQ),
-             ((Q6, 32000, 4096, 2), qmm.QMM_PATH_FUSED_MMVQ), ((Q6, 4096, 4096, 8), qmm.QMM_PATH_MMVQ),
-             ((Q6, 4096, 4096, 9), qmm.QMM_PATH_MMQ), ((Q6, 32000, 4096, 80), qmm.QMM_PATH_MMQ)]
+    F, V, G = qmm.QMM_PATH_FUSED_MMVQ, qmm.QMM_PATH_MMVQ, qmm.QMM_PATH_MMQ
+    cases = [((Q4, 4096, 4096, 1), F), ((Q4, 11008, 4096, 1), F), ((Q4, 256, 512, 4), F),
+             ((Q4, 4096, 4096, 4), F), ((Q4, 4096, 4096, 5), V), ((Q4, 4096, 4096, 8), V),
+             ((Q4, 4096, 14336, 2), F), ((Q4, 4096, 14336, 4), V), ((Q4, 4096, 14336, 8), V),
+             ((Q4, 14336, 16384, 3), V), ((Q4, 4096, 4096, 9), V), ((Q4, 4096, 4096, 16), V),
+             ((Q4, 4096, 4096, 17), G), ((Q4, 4096, 4096, 512), G), ((Q6, 4096, 4096, 1), F),
+             ((Q6, 32000, 4096, 2), V), ((Q6, 4096, 4096, 8), V), ((Q6, 4096, 4096, 9), V),
+             ((Q6, 4096, 4096, 17), G), ((Q6, 32000, 4096, 80), G)]
     for args, path in cases:
         assert qmm.qmm_matmul_path(*args) == path, args
         assert (qmm.qmm_matmul_workspace_bytes(*args) > 0) == (path == qmm.QMM_PATH_MMQ), args

@@ -125,12 +125,30 @@ def test_gemm_block_dots_bit_exact(qtype, od, K, nt):
     assert np.array_equal(d.cpu().numpy(), ora().block_dots(qtype, W, xq, od))
 
 
+@pytest.mark.parametrize("qtype,od,K,nt", [(Q4_K, 256, 512, 1), (Q4_K, 300, 768, 3), (Q4_K, 1000, 4096, 8),
+                                           (Q4_K, 17, 14336, 8), (Q4_K, 4096, 4096, 13), (Q4_K, 33, 2304, 16),
+                                           (Q6_K, 256, 2048, 2), (Q6_K, 300, 4096, 8), (Q6_K, 33, 6144, 12), (Q6_K, 33, 4096, 16),
+                                           (Q6_K, 1, 2048, 5), (Q6_K, 4096, 4096, 11)])
+def test_mma_block_dots_bit_exact(qtype, od, K, nt):
+    """The warp-MMA MMVQ dot code (subnormal-f16 weight codes times f16
+    activation codes, f32 accumulation): every block dot exact.  Shapes cover
+    a ragged last row tile, a K that ends inside a 2048-k stage, the raw-byte
+    activation layout (K = 14336) and 9..16 tokens (two token tiles)."""
+    W, x = _case(qtype, od, K, nt, seed=od + 3 * nt)
+    xq, xds = ora().quantize_q8_1(x)
+    d = qmm.block_dots(qtype, dev(W, torch), dev(xq, torch), dev(xds, torch), od, path=2)
+    torch.cuda.synchronize()
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+    assert np.array_equal(d.cpu().numpy(), ora().block_dots(qtype, W, xq, od))
+
+
 # ---------------------------------------------------------------- GEMV ---
 
 @pytest.mark.parametrize("od,K,nt", [(256, 512, 1), (256, 512, 8), (1000, 768, 5), (1, 256, 2),
                                      (4096, 4096, 1), (11008, 4096, 1), (14336, 4096, 2),
                                      (14336, 4096, 4), (14336, 4096, 8), (4096, 14336, 2),
-                                     (4096, 14336, 4), (4096, 14336, 8)])
+                                     (4096, 14336, 4), (4096, 14336, 8), (4096, 4096, 16), (1000, 768, 11),
+                                     (300, 4096, 13)])
 def test_gemv_matches_oracle(od, K, nt):
     W, x = _case(Q4_K, od, K, nt, outliers=(nt == 1), seed=0)
     xq, xds = ora().quantize_q8_1(x)
@@ -140,7 +158,8 @@ def test_gemv_matches_oracle(od, K, nt):
 
 
 @pytest.mark.parametrize("od,K,nt", [(256, 2048, 1), (1000, 4096, 5), (4096, 4096, 8), (129, 6144, 2),
-                                     (32000, 4096, 1), (33, 2048, 7)])
+                                     (32000, 4096, 1), (33, 2048, 7), (4096, 4096, 16), (32000, 4096, 8),
+                                     (257, 2048, 12)])
 def test_gemv_q6k_matches_oracle(od, K, nt):
     W, x = _case(Q6_K, od, K, nt, outliers=(nt == 1), seed=2)
     xq, xds = ora().quantize_q8_1(x)
@@ -150,11 +169,15 @@ def test_gemv_q6k_matches_oracle(od, K, nt):
     assert_close_rows(out[:, rows] if od > 4096 else out, ref, f"q6k gemv {od}x{K} nt={nt}")
 
 
-@pytest.mark.parametrize("od,K,nt", [(4096, 4096, 1), (300, 2048, 3), (32000, 4096, 2), (1000, 2048, 4)])
-def test_fused_q6k_matmul(od, K, nt):
-    """Q6_K decode shapes take the fused quantize + MMVQ kernel: q8_1 outputs
+@pytest.mark.parametrize("od,K,nt,path", [(4096, 4096, 1, qmm.QMM_PATH_FUSED_MMVQ),
+                                          (32000, 4096, 1, qmm.QMM_PATH_FUSED_MMVQ),
+                                          (300, 2048, 3, qmm.QMM_PATH_MMVQ), (32000, 4096, 2, qmm.QMM_PATH_MMVQ),
+                                          (1000, 2048, 4, qmm.QMM_PATH_MMVQ)])
+def test_q6k_matmul_small_batch(od, K, nt, path):
+    """Q6_K small-batch shapes through qmm_matmul: the fused quantize + dp4a
+    MMVQ at nt = 1, quantize + the warp-MMA MMVQ from 2 tokens.  q8_1 outputs
     bit-exact, outputs within tolerance."""
-    assert qmm.qmm_matmul_path(Q6_K, od, K, nt) == qmm.QMM_PATH_FUSED_MMVQ
+    assert qmm.qmm_matmul_path(Q6_K, od, K, nt) == path
     W, x = _case(Q6_K, od, K, nt, outliers=True, seed=od)
     out, xq, xds = qmm.matmul(Q6_K, dev(W, torch), dev(x, torch), od, flags=qmm.QMM_FLAG_STATIC_WEIGHTS,
                               return_q8=True)
@@ -214,10 +237,12 @@ def test_workload_skinny_q6k(case):
                                            (129, 2304, 2, 0), (2048, 4096, 8, 1), (1000, 2048, 6, 0),
                                            (300, 14336, 2, 1), (777, 1280, 7, 0), (4096, 4096, 5, 1)])
 def test_fused_quantize_matmul(od, K, nt, flags):
-    """The fused quantize + MMVQ kernel (decode and small-batch shapes): q8_1
-    outputs bit-exact, matmul output within tolerance, with and without the
-    static-weights flag."""
-    assert qmm.qmm_matmul_path(Q4_K, od, K, nt) == qmm.QMM_PATH_FUSED_MMVQ
+    """qmm_matmul on the decode and small-batch shapes -- the fused quantize +
+    dp4a MMVQ kernel up to 4 tokens, quantize + the warp-MMA MMVQ from 5:
+    q8_1 outputs bit-exact, matmul output within tolerance, with and without
+    the static-weights flag."""
+    want = qmm.QMM_PATH_FUSED_MMVQ if nt <= 4 else qmm.QMM_PATH_MMVQ
+    assert qmm.qmm_matmul_path(Q4_K, od, K, nt) == want
     W, x = _case(Q4_K, od, K, nt, outliers=True, seed=od + K)
     out, xq, xds = qmm.matmul(Q4_K, dev(W, torch), dev(x, torch), od, flags=flags, return_q8=True)
     oq, ods = ora().quantize_q8_1(x)
