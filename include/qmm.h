@@ -162,8 +162,8 @@ int qmm_gemm(int qtype, const void *W, const int8_t *xq, const float *xds, float
  * compiled into the library and reserved on each device when the library's
  * module loads.  The function itself allocates nothing.
  *   - Size limit: qmm_gemm_workspace_bytes(qtype, od, K, nt) must not exceed
- *     QMM_BUILTIN_WORKSPACE_BYTES (e.g. nt = 512 at K = 4096 needs 4.5 MiB;
- *     nt = 512 at K = 14336 needs 15.75 MiB and is refused).  A larger problem
+ *     QMM_BUILTIN_WORKSPACE_BYTES (e.g. nt = 512 at K = 4096 needs 4.75 MiB;
+ *     nt = 512 at K = 14336 needs 16.6 MiB and is refused).  A larger problem
  *     returns QMM_EWORKSPACE and launches nothing; use qmm_gemm with a
  *     workspace of your own for it.
  *   - Nothing in the array has to start at zero: the prepass rewrites every

@@ -328,15 +328,18 @@ extern "C" int qmm_gemm_builtin_workspace(int qtype, const void* W, const int8_t
   rc = builtin_ws_ptr(&ws);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The prepass writes the scale rows only for tokens < nt; the padding
+  // The prepass writes the scale planes only for tokens < nt; the padding
   // tokens of the last tile would otherwise hold whatever an earlier call of
   // another shape left there.  They feed only output columns that are never
   // stored, but they are zeroed so every call computes on defined values.
   const int64_t ntp = gemm_ntp(nt);
   if (ntp > nt) {
-    uint8_t* scl = static_cast<uint8_t*>(ws) + gemm_xh_bytes(nt, K);
-    if (cudaMemset2DAsync(scl + nt * 8, (size_t)ntp * 8, 0, (size_t)(ntp - nt) * 8, (size_t)(K / 32), st) !=
-        cudaSuccess)
+    uint8_t* dxp = static_cast<uint8_t*>(ws) + gemm_xh_bytes(nt, K);
+    uint8_t* smp = dxp + gemm_dx_bytes(nt, K);
+    if (cudaMemset2DAsync(dxp + nt * 4, (size_t)ntp * 4, 0, (size_t)(ntp - nt) * 4, (size_t)(K / 32), st) !=
+            cudaSuccess ||
+        cudaMemset2DAsync(smp + nt * 16, (size_t)ntp * 16, 0, (size_t)(ntp - nt) * 16, (size_t)(K / 256) * 4, st) !=
+            cudaSuccess)
       return QMM_ELAUNCH;
   }
   return gemm_core(qtype, W, xq, xds, out, nullptr, od, K, nt, ws, (size_t)QMM_BUILTIN_WORKSPACE_BYTES, true, st);

@@ -58,14 +58,23 @@ struct Cfg {
   static constexpr int RAW_BYTES = BM * RAW_ROW;
   static constexpr int A_BYTES = BM * KS * 2;
   static constexpr int B_BYTES = BN * KS * 2;
-  static constexpr int SC_BYTES = 2 * BN * 8;
+  static constexpr int SC_BYTES = 2 * BN * 4;  // dx of the stage's two 32-k groups
+  // Q4_K min term: per super-block the MMA operands m[row][8p + j] (A) and
+  // s_p[token][8p + j] (B, the three bf16 parts of s), k = 32: 4 chunks of 8
+  static constexpr bool MINMMA = QT == kQ4;
+  static constexpr int AMIN_BYTES = MINMMA ? BM * 64 : 0;
+  static constexpr int BMIN_BYTES = MINMMA ? BN * 64 : 0;
+  // TMEM: NBUF group accumulators of BN columns, then the min-term accumulator
+  static constexpr int NBUF = MINMMA ? 3 : 4;
   static constexpr int RAW_OFF = 0;
   static constexpr int A_OFF = RAW_OFF + RS * RAW_BYTES;
   static constexpr int B_OFF = A_OFF + AS * A_BYTES;
   static constexpr int SC_OFF = B_OFF + BS * B_BYTES;
-  static constexpr int BAR_OFF = SC_OFF + BS * SC_BYTES;
-  // barriers: raw full/empty, a full/empty, b full/empty, acc full/empty, done
-  static constexpr int NBARS = 2 * RS + 2 * AS + 2 * BS + 8 + 1;
+  static constexpr int AMIN_OFF = SC_OFF + BS * SC_BYTES;
+  static constexpr int BMIN_OFF = AMIN_OFF + RS * AMIN_BYTES;
+  static constexpr int BAR_OFF = BMIN_OFF + RS * BMIN_BYTES;
+  // barriers: raw full/empty, a full/empty, b full/empty, acc full/empty, done, min full/empty
+  static constexpr int NBARS = 2 * RS + 2 * AS + 2 * BS + 8 + 1 + 2;
   static constexpr int SMEM = BAR_OFF + NBARS * 8 + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr int TMEM_COLS = 4 * BN;
   static_assert(RAW_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
@@ -84,6 +93,8 @@ struct Bars {
   __device__ uint32_t acc_full(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + i); }
   __device__ uint32_t acc_empty(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 4 + i); }
   __device__ uint32_t done() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 8); }
+  __device__ uint32_t min_full() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 9); }
+  __device__ uint32_t min_empty() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 10); }
 };
 
 // Wait used while draining: ignores the abort flag, gives up at `deadline`.
@@ -190,7 +201,7 @@ __device__ __forceinline__ void unpack_q6k_stage(const uint8_t* row_window, int 
 template <int QT, int BN, bool DOTS>
 __global__ void __launch_bounds__(384, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const float2* __restrict__ scl, const uint8_t* __restrict__ W, float* __restrict__ out,
+                   const float* __restrict__ scl, const uint8_t* __restrict__ W, float* __restrict__ out,
                    int32_t* __restrict__ dots, int od, int K, int nt, int ntp, int* status, int limit_ms,
                    int skip_first_weight_load) {
   using C = Cfg<QT, BN>;
@@ -215,7 +226,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::RS; ++i) {
       mbar_init(bars.raw_full(i), 1);
-      mbar_init(bars.raw_empty(i), 2);
+      mbar_init(bars.raw_empty(i), C::MINMMA && !DOTS ? 3 : 2);  // unpack warps (+ the min-term MMAs)
     }
     for (int i = 0; i < C::AS; ++i) {
       mbar_init(bars.a_full(i), 2);
@@ -230,6 +241,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bars.acc_empty(i), 8);
     }
     mbar_init(bars.done(), 1);
+    mbar_init(bars.min_full(), 1);
+    mbar_init(bars.min_empty(), 8);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -249,6 +262,10 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   const uint32_t raw_s = sb + C::RAW_OFF, a_s = sb + C::A_OFF, b_s = sb + C::B_OFF, sc_s = sb + C::SC_OFF;
+  const uint32_t amin_s = sb + C::AMIN_OFF, bmin_s = sb + C::BMIN_OFF;
+  // the bf16 parts of s: [K/256][4][ntp][8] after the dx plane [K/32][ntp]
+  const uint8_t* smin = reinterpret_cast<const uint8_t*>(scl + (size_t)(K >> 5) * ntp);
+  constexpr bool MIN = C::MINMMA && !DOTS;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -260,9 +277,15 @@ __global__ void __launch_bounds__(384, 1)
         const int rs = b % C::RS;
         if (!wait_bar(bars.raw_empty(rs), ((b / C::RS) & 1) ^ 1, g)) break;
         if (!(skip_first_weight_load && b == 0)) {
-          mbar_arrive_expect_tx(bars.raw_full(rs), C::RAW_BYTES);
+          mbar_arrive_expect_tx(bars.raw_full(rs), C::RAW_BYTES + (MIN ? 4 * BN * 16 : 0));
           const int x = QT == kQ4 ? (b + b_off) * kQ4KBytes : ((b + b_off) * kQ6KBytes) & ~15;
           tma_load_2d(raw_s + rs * C::RAW_BYTES, &tmW, x, row0, bars.raw_full(rs));
+          if (MIN) {
+#pragma unroll
+            for (int kc = 0; kc < 4; ++kc)
+              bulk_load(bmin_s + rs * C::BMIN_BYTES + kc * BN * 16,
+                        smin + (((size_t)(b + b_off) * 4 + kc) * ntp + tok0) * 16, BN * 16, bars.raw_full(rs));
+          }
         }
         ++raw_issued;
         for (int s = 0; s < 4; ++s) {
@@ -276,8 +299,8 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_2d(b_s + bs * C::B_BYTES, &tmX, C::KS * gk, tok0, bars.b_full(bs));
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi)
-            bulk_load(sc_s + bs * C::SC_BYTES + gi * BN * 8, scl + ((size_t)(2 * gk + gi) * ntp + tok0),
-                      BN * 8, bars.b_full(bs));
+            bulk_load(sc_s + bs * C::SC_BYTES + gi * BN * 4, scl + ((size_t)(2 * gk + gi) * ntp + tok0),
+                      BN * 4, bars.b_full(bs));
           ++b_issued;
         }
       }
@@ -301,8 +324,8 @@ __global__ void __launch_bounds__(384, 1)
         if (!wait_bar(bars.b_full(bs), (gs / C::BS) & 1, g)) break;
         tc_fence_after();
         for (int gi = 0; gi < C::GPS; ++gi, ++u) {
-          const int buf = u & 3;
-          if (!wait_bar(bars.acc_empty(buf), ((u >> 2) & 1) ^ 1, g)) {
+          const int buf = u % C::NBUF;
+          if (!wait_bar(bars.acc_empty(buf), ((u / C::NBUF) & 1) ^ 1, g)) {
             ok = false;
             break;
           }
@@ -319,6 +342,23 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         tc_commit(bars.a_empty(as));
         tc_commit(bars.b_empty(bs));
+        if (MIN && (gs & 3) == 3) {
+          // super-block b: D_min[r][t] = sum over its 8 sub-blocks j of
+          // m[r][j] * s[t][j], with s split into three bf16 parts (exact
+          // products, f32 sums); then the raw stage (and these operands) may go
+          const int b = gs >> 2, rs = b % C::RS;
+          if (!wait_bar(bars.min_empty(), (b & 1) ^ 1, g)) break;
+          tc_fence_after();
+          const uint32_t idesc_bf = idesc_f16(C::BM, BN) | (1u << 7) | (1u << 10);  // A and B bf16
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t ad = smem_desc(amin_s + rs * C::AMIN_BYTES + kk * 4096, 2048, 128, 0);
+            const uint64_t bd = smem_desc(bmin_s + rs * C::BMIN_BYTES + kk * 2 * BN * 16, BN * 16, 128, 0);
+            tc_mma_f16(tmem + (uint32_t)(C::NBUF * BN), ad, bd, idesc_bf, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bars.min_full());
+          tc_commit(bars.raw_empty(rs));
+        }
       }
       tc_commit(bars.done());
       drain_wait(bars.done(), 0, global_ns() + 1000000000ull);
@@ -338,6 +378,28 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         uint8_t* a = smem + C::A_OFF + as * C::A_BYTES;
+        if (MIN && s == 0) {
+          // m[r][j] of the 8 sub-blocks as bf16 (exact small integers), the
+          // same 16 bytes for parts 0, 1, 2, zeros for the fourth chunk
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int r = ut + 64 * rr;
+            const uint4 hdr = *reinterpret_cast<const uint4*>(raw + r * C::RAW_ROW);
+            uint32_t mw[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              uint32_t sc2, m2;
+              q4k_pair_codes(hdr.y, hdr.z, hdr.w, p, sc2, m2);
+              mw[p] = (__float_as_uint((float)(m2 & 0xFFu)) >> 16) | (__float_as_uint((float)(m2 >> 8)) & 0xFFFF0000u);
+            }
+            uint8_t* am = smem + C::AMIN_OFF + rs * C::AMIN_BYTES + r * 16;
+            const uint4 v = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+            *reinterpret_cast<uint4*>(am) = v;
+            *reinterpret_cast<uint4*>(am + 2048) = v;
+            *reinterpret_cast<uint4*>(am + 4096) = v;
+            *reinterpret_cast<uint4*>(am + 6144) = make_uint4(0, 0, 0, 0);
+          }
+        }
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
           const int r = ut + 64 * rr;
@@ -388,7 +450,7 @@ __global__ void __launch_bounds__(384, 1)
     };
     fetch_scales(0);
     for (int b = 0; b < nsb && ok; ++b) {
-      float gcoef[QT == kQ4 ? 8 : 16];  // per-group coefficient (min term or scale)
+      float gcoef[QT == kQ4 ? 1 : 16];  // Q4_K: -dmin / sigma; Q6_K: the groups' scales
       if (!DOTS) {
         const uint4 hdr = hdr_next;
         uint32_t sw[9];
@@ -407,13 +469,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         if (QT == kQ4) {
-          const float dmin_s = half_bits_to_float(hdr.x >> 16) * __fdividef(1.0f, sigma);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            int sc, m;
-            q4k_scale_min_words(hdr.y, hdr.z, hdr.w, j, sc, m);
-            gcoef[j] = -dmin_s * (float)m;
-          }
+          gcoef[0] = -half_bits_to_float(hdr.x >> 16) * __fdividef(1.0f, sigma);  // -dmin / sigma
         } else {
 #pragma unroll
           for (int gg = 0; gg < 16; ++gg) {
@@ -432,47 +488,42 @@ __global__ void __launch_bounds__(384, 1)
         const float* scp = reinterpret_cast<const float*>(smem + C::SC_OFF + bs * C::SC_BYTES);
 #pragma unroll
         for (int gi = 0; gi < C::GPS; ++gi, ++u) {
-          const int buf = u & 3;
-          if (!warp_wait(bars.acc_full(buf), (u >> 2) & 1, g)) {
+          const int buf = u % C::NBUF;
+          if (!warp_wait(bars.acc_full(buf), (u / C::NBUF) & 1, g)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          uint32_t P[CH][32];
+          // one 32-column chunk at a time: load, wait, use (32 live
+          // registers of TMEM data instead of BN/2, so nothing spills)
+          const int sub = QT == kQ4 ? gi : (gi >> 1);  // 32-value sub-block within the stage
+          const float* sg = scp + sub * BN + hc * HALF;  // dx of this group's tokens
+          const float coef = DOTS || QT == kQ4 ? 1.0f : gcoef[4 * s + gi];
 #pragma unroll
-          for (int c = 0; c < CH; ++c)
-            tc_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + hc * HALF + 32 * c), P[c]);
-#pragma unroll
-          for (int c = 0; c < CH; ++c) tc_wait_ld(P[c]);
-          if (DOTS) {
-            const int ng = QT == kQ4 ? (K >> 5) : (K >> 4);
-            const int grp = QT == kQ4 ? 8 * (b + b_off) + 2 * s + gi : 16 * (b + b_off) + 4 * s + gi;
-#pragma unroll
-            for (int c = 0; c < CH; ++c)
+          for (int c = 0; c < CH; ++c) {
+            uint32_t P[32];
+            __syncwarp();
+            tc_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + hc * HALF + 32 * c), P);
+            tc_wait_ld(P);
+            if (DOTS) {
+              const int ng = QT == kQ4 ? (K >> 5) : (K >> 4);
+              const int grp = QT == kQ4 ? 8 * (b + b_off) + 2 * s + gi : 16 * (b + b_off) + 4 * s + gi;
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 const int t = tok0 + hc * HALF + 32 * c + i;
                 if (row_ok && t < nt)
-                  dots[((size_t)t * od + row_g) * ng + grp] = __float2int_rn(__uint_as_float(P[c][i]));
+                  dots[((size_t)t * od + row_g) * ng + grp] = __float2int_rn(__uint_as_float(P[i]));
               }
-          } else {
-            const int sub = QT == kQ4 ? gi : (gi >> 1);  // 32-value sub-block within the stage
-            const float* sg = scp + sub * BN * 2 + hc * HALF * 2;
-            const float coef = gcoef[QT == kQ4 ? 2 * s + gi : 4 * s + gi];
+            } else {
 #pragma unroll
-            for (int c = 0; c < CH; ++c)
+              for (int i = 0; i < 32; i += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(sg + 32 * c + i);
+                const float dx[4] = {v.x * coef, v.y * coef, v.z * coef, v.w * coef};
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                const float4 v = *reinterpret_cast<const float4*>(sg + 2 * (32 * c + i));  // dx0 s0 dx1 s1
-                const float p0 = __uint_as_float(P[c][i]), p1 = __uint_as_float(P[c][i + 1]);
-                if (QT == kQ4) {
-                  acc[32 * c + i] = fmaf(coef, v.y, fmaf(v.x, p0, acc[32 * c + i]));
-                  acc[32 * c + i + 1] = fmaf(coef, v.w, fmaf(v.z, p1, acc[32 * c + i + 1]));
-                } else {
-                  acc[32 * c + i] = fmaf(v.x * coef, p0, acc[32 * c + i]);
-                  acc[32 * c + i + 1] = fmaf(v.z * coef, p1, acc[32 * c + i + 1]);
-                }
+                for (int e = 0; e < 4; ++e)
+                  acc[32 * c + i + e] = fmaf(dx[e], __uint_as_float(P[i + e]), acc[32 * c + i + e]);
               }
+            }
           }
           // hand the accumulator back only now, after its values were used
           tc_fence_before();
@@ -482,6 +533,28 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.b_empty(bs));
+      }
+      if (MIN && ok) {
+        // the super-block's min term: acc += (-dmin / sigma) * D_min
+        if (!warp_wait(bars.min_full(), b & 1, g)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float mc = gcoef[0];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          uint32_t Q[32];
+          __syncwarp();
+          tc_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::NBUF * BN + hc * HALF + 32 * c), Q);
+          tc_wait_ld(Q);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(mc, __uint_as_float(Q[i]), acc[32 * c + i]);
+        }
+        // hand the accumulator back only after its values were used
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.min_empty());
       }
     }
     if (!DOTS && ok && row_ok) {
@@ -556,7 +629,7 @@ int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, in
   const dim3 grid((unsigned)((od + C::BM - 1) / C::BM), (unsigned)((nt + BN - 1) / BN), (unsigned)S);
   const int limit_ms = stall_ms > 0 ? stall_ms : 4000;
   gemm_tc_kernel<QT, BN, DOTS><<<grid, 384, C::SMEM, stream>>>(
-      mw, mx, reinterpret_cast<const float2*>(scl), static_cast<const uint8_t*>(W), S > 1 ? part : out, dots,
+      mw, mx, scl, static_cast<const uint8_t*>(W), S > 1 ? part : out, dots,
       (int)od, (int)K, (int)nt, (int)gemm_ntp(nt), status, limit_ms, stall_ms > 0 ? 1 : 0);
   if (cudaGetLastError() != cudaSuccess) return QMM_ELAUNCH;
   if (S > 1) {

@@ -13,15 +13,20 @@
 
 namespace qmm {
 
-// Layout of the tensor-core GEMM workspace: f16 codes [nt][K], then the
-// token-contiguous scale rows [K/32][ntp] float2.  ntp pads nt to a whole
-// number of the widest token tile so every bulk copy stays in bounds.
+// Layout of the tensor-core GEMM workspace: f16 codes [nt][K]; the scale
+// planes -- the token-contiguous dx rows [K/32][ntp] f32, then for the Q4_K
+// min term the three bf16 parts of s per super-block [K/256][4][ntp][8]
+// (chunk p < 3: part p of s for the super-block's 8 blocks; chunk 3: zero);
+// then the split-K partial sums.  ntp pads nt to a whole number of the widest
+// token tile so every bulk copy stays in bounds.
 constexpr int64_t kMaxTokenTile = 256;
 inline int64_t gemm_ntp(int64_t nt) { return (nt + kMaxTokenTile - 1) / kMaxTokenTile * kMaxTokenTile; }
 inline size_t gemm_xh_bytes(int64_t nt, int64_t K) {
   return (size_t)((nt * K * 2 + 255) / 256 * 256);
 }
-inline size_t gemm_scl_bytes(int64_t nt, int64_t K) { return (size_t)(K / 32) * gemm_ntp(nt) * 8; }
+inline size_t gemm_dx_bytes(int64_t nt, int64_t K) { return (size_t)(K / 32) * gemm_ntp(nt) * 4; }
+inline size_t gemm_smin_bytes(int64_t nt, int64_t K) { return (size_t)(K / 256) * 4 * gemm_ntp(nt) * 16; }
+inline size_t gemm_scl_bytes(int64_t nt, int64_t K) { return gemm_dx_bytes(nt, K) + gemm_smin_bytes(nt, K); }
 
 // Split-K factor of the tensor-core GEMM, a function of the shape alone: a
 // grid of fewer 128-row x token tiles than the 152 SMs of a GB300 takes its K

@@ -13,19 +13,46 @@
 
 namespace qmm {
 
+// bf16 bits of v rounded to nearest even (v finite).
+__device__ __forceinline__ uint32_t bf16_rn_bits(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+// Scale planes of one (token t, block j) for the tensor-core GEMM: d into
+// the dx plane, and s = s0 + s1 + s2 exactly as three bf16 (each part takes
+// the next 8 significant bits of the remainder: the remainders are exact in
+// f32 and the third part holds the last at most 8 bits) into the min-term
+// planes, chunk 3 zero.
+__device__ __forceinline__ void write_gemm_scales(float* scl, int64_t nb, int64_t ntp, int64_t t, int64_t j,
+                                                  float d, float s) {
+  scl[j * ntp + t] = d;
+  uint16_t* sm = reinterpret_cast<uint16_t*>(scl + nb * ntp);
+  const uint32_t p0 = bf16_rn_bits(s);
+  const float r0 = s - __uint_as_float(p0 << 16);
+  const uint32_t p1 = bf16_rn_bits(r0);
+  const uint32_t p2 = bf16_rn_bits(r0 - __uint_as_float(p1 << 16));
+  const int64_t base = ((j >> 3) * 4 * ntp + t) * 8 + (j & 7);  // chunk 0 of super-block j/8
+  sm[base] = (uint16_t)p0;
+  sm[base + ntp * 8] = (uint16_t)p1;
+  sm[base + 2 * ntp * 8] = (uint16_t)p2;
+  sm[base + 3 * ntp * 8] = 0;
+}
+
 // Eight lanes per 32-value block, four values per lane (one 16-byte load);
 // a warp takes four blocks per step, grid-stride over all nt*K/32 blocks.
 // The block maximum and the code sum are 3-step shuffle reductions within the
 // eight lanes; d = amax/127 by IEEE division, the codes by q8_codes (the
 // same integers IEEE division and round-half-even give), s = d * sum(q).
 // When xh / scl are non-null the same pass also writes the tensor-core GEMM
-// operands: the codes as exact f16 (xh [nt][K]) and the scales token-
-// contiguous (scl [K/32][ntp] float2 = (d, s)).
+// operands (the workspace layout of qmm_internal.h): the codes as exact f16
+// (xh [nt][K]), d token-contiguous (scl [K/32][ntp]) and s as three bf16
+// parts for the min-term MMA.
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restrict__ x, int64_t nblocks,
                                                             int64_t nb_per_row, int8_t* __restrict__ xq,
                                                             float2* __restrict__ xds,
                                                             __half* __restrict__ xh,
-                                                            float2* __restrict__ scl, int64_t ntp) {
+                                                            float* __restrict__ scl, int64_t ntp) {
   const int lane = threadIdx.x & 31, q8 = lane & 7;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   // wait until the preceding grid is done (it may write x or read xq / xds),
@@ -63,22 +90,19 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restr
       }
       if (q8 == 0) {
         xds[b] = make_float2(d, s);
-        if (scl) {
-          const int64_t t = b / nb_per_row, j = b % nb_per_row;
-          scl[j * ntp + t] = make_float2(d, s);
-        }
+        if (scl) write_gemm_scales(scl, nb_per_row, ntp, b / nb_per_row, b % nb_per_row, d, s);
       }
     }
   }
 }
 
 // Prepass for qmm_gemm when the caller already holds xq / xds: 16 codes per
-// thread to f16, and the (d, s) pairs transposed to token-contiguous rows.
+// thread to f16, and the scale planes (as the quantizer writes them).
 __global__ void __launch_bounds__(256) gemm_operand_prep_kernel(const int8_t* __restrict__ xq,
                                                                 const float2* __restrict__ xds, int64_t nt,
                                                                 int64_t K, int64_t ntp,
                                                                 __half* __restrict__ xh,
-                                                                float2* __restrict__ scl) {
+                                                                float* __restrict__ scl) {
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t n16 = nt * K / 16;
@@ -103,7 +127,8 @@ __global__ void __launch_bounds__(256) gemm_operand_prep_kernel(const int8_t* __
   const int64_t nscl = nt * nb;
   for (int64_t i = tid; i < nscl; i += stride) {
     const int64_t t = i / nb, j = i % nb;
-    scl[j * ntp + t] = __ldg(xds + i);
+    const float2 ds = __ldg(xds + i);
+    write_gemm_scales(scl, nb, ntp, t, j, ds.x, ds.y);
   }
 }
 
@@ -119,15 +144,14 @@ int launch_quantize(const float* x, int64_t nt, int64_t K, int8_t* xq, float* xd
   const int64_t nblocks = nt * (K / 32);
   if (nblocks == 0) return QMM_OK;
   return launch_ex(quantize_q8_1_kernel, dim3(grid_for(nblocks, 32)), dim3(256), 0, stream, true, x, nblocks,
-                    (int64_t)(K / 32), xq, reinterpret_cast<float2*>(xds), xh, reinterpret_cast<float2*>(scl),
-                    ntp);
+                    (int64_t)(K / 32), xq, reinterpret_cast<float2*>(xds), xh, scl, ntp);
 }
 
 int launch_gemm_prep(const int8_t* xq, const float* xds, int64_t nt, int64_t K, int64_t ntp, __half* xh,
                      float* scl, cudaStream_t stream) {
   const int64_t work = nt * K / 16;
   gemm_operand_prep_kernel<<<grid_for(work, 256), 256, 0, stream>>>(
-      xq, reinterpret_cast<const float2*>(xds), nt, K, ntp, xh, reinterpret_cast<float2*>(scl));
+      xq, reinterpret_cast<const float2*>(xds), nt, K, ntp, xh, scl);
   return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ELAUNCH;
 }
 

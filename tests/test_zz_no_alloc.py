@@ -27,9 +27,9 @@ def test_size_limit_is_refused_before_any_device_work():
     big = (Q4_K, 4096, 14336, 512)
     assert qmm.qmm_gemm_workspace_bytes(*big) > qmm.QMM_BUILTIN_WORKSPACE_BYTES
     assert qmm.qmm_gemm_builtin_workspace(Q4_K, p, p, p, p, 4096, 14336, 512, 0) == qmm.QMM_EWORKSPACE
-    # nt = 896 at K = 4096 fills the array exactly; one token more does not fit
-    assert qmm.qmm_gemm_workspace_bytes(Q4_K, 4096, 4096, 896) == qmm.QMM_BUILTIN_WORKSPACE_BYTES
-    assert qmm.qmm_gemm_builtin_workspace(Q4_K, p, p, p, p, 4096, 4096, 897, 0) == qmm.QMM_EWORKSPACE
+    # nt = 832 at K = 4096 fills the array exactly; one token more does not fit
+    assert qmm.qmm_gemm_workspace_bytes(Q4_K, 4096, 4096, 832) == qmm.QMM_BUILTIN_WORKSPACE_BYTES
+    assert qmm.qmm_gemm_builtin_workspace(Q4_K, p, p, p, p, 4096, 4096, 833, 0) == qmm.QMM_EWORKSPACE
     assert qmm.qmm_gemm_builtin_workspace(Q4_K, p, p, p, p, 4096, 300, 8, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_gemm_builtin_workspace(Q4_K, 0, p, p, p, 4096, 4096, 8, 0) == qmm.QMM_ENULL
     assert qmm.qmm_gemm_builtin_workspace(9, p, p, p, p, 4096, 4096, 8, 0) == qmm.QMM_EINVAL_QTYPE
@@ -46,7 +46,7 @@ def test_builtin_workspace_matches_qmm_gemm():
     torch = pytest.importorskip("torch")
     # the largest shape first, so the later, smaller ones run on scratch that
     # holds another layout's leftovers
-    shapes = [(Q4_K, 4096, 4096, 896), (Q4_K, 300, 512, 70), (Q6_K, 4096, 4096, 64), (Q4_K, 1000, 2048, 9)]
+    shapes = [(Q4_K, 4096, 4096, 832), (Q4_K, 300, 512, 70), (Q6_K, 4096, 4096, 64), (Q4_K, 1000, 2048, 9)]
     assert qmm.qmm_gemm_workspace_bytes(*shapes[0]) == qmm.QMM_BUILTIN_WORKSPACE_BYTES
     st = torch.cuda.current_stream().cuda_stream
     for qtype, od, K, nt in shapes:
