@@ -20,8 +20,9 @@
 //               activation tile (BN x 64, 128-byte swizzle) and the
 //               token-contiguous (dx, s) rows of the same 64 k.
 //   warp 1      TMEM allocation and the single MMA-issuing thread: per scale
-//               group an MMA chain into one of four TMEM accumulators (round
-//               robin by group), committed to an mbarrier.
+//               group an MMA chain into one of NBUF TMEM accumulators (3 to 8
+//               of the 512 columns; round robin by group), committed to an
+//               mbarrier.
 //   warps 2-3   unpack: raw nibbles / 6-bit codes -> f16 operand tiles in the
 //               canonical no-swizzle K-major layout (Q4_K folds the 6-bit scale
 //               into the operand: sc*nibble is exact), one 64-k stage at a time.
@@ -50,6 +51,14 @@ constexpr int kQ4 = 0, kQ6 = 1;
 template <int QT, int BN>
 struct Cfg {
   static constexpr int BM = 128;
+  // unpack warps.  Four (14 warps) would halve Q6_K's unpack time, but that
+  // layout returned wrong sums in a few per cent of back-to-back Q6_K calls
+  // (one epilogue warp's 32 rows x 4 tokens), with either epilogue form and
+  // either accumulator count; with two every repeat is bit-identical.
+  static constexpr int NU = 2;
+  static constexpr int UROWS = BM / (32 * NU);  // rows each unpack thread converts per stage
+  static constexpr int EPI0 = 2 + NU;           // first of the 8 epilogue warps
+  static constexpr int THREADS = 32 * (EPI0 + 8);
   static constexpr int KS = 64;  // k per operand stage
   static constexpr int RS = 2, AS = 3, BS = 4;
   static constexpr int RAW_ROW = QT == kQ4 ? 144 : 224;
@@ -64,8 +73,11 @@ struct Cfg {
   static constexpr bool MINMMA = QT == kQ4;
   static constexpr int AMIN_BYTES = MINMMA ? BM * 64 : 0;
   static constexpr int BMIN_BYTES = MINMMA ? BN * 64 : 0;
-  // TMEM: NBUF group accumulators of BN columns, then the min-term accumulator
-  static constexpr int NBUF = MINMMA ? 3 : 4;
+  // TMEM (all 512 columns): NBUF group accumulators of BN columns, then the
+  // min-term accumulator
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NBUF = TMEM_COLS / BN - (MINMMA ? 1 : 0);
+  static_assert(NBUF <= 8, "accumulator barriers");
   static constexpr int RAW_OFF = 0;
   static constexpr int A_OFF = RAW_OFF + RS * RAW_BYTES;
   static constexpr int B_OFF = A_OFF + AS * A_BYTES;
@@ -74,9 +86,8 @@ struct Cfg {
   static constexpr int BMIN_OFF = AMIN_OFF + RS * AMIN_BYTES;
   static constexpr int BAR_OFF = BMIN_OFF + RS * BMIN_BYTES;
   // barriers: raw full/empty, a full/empty, b full/empty, acc full/empty, done, min full/empty
-  static constexpr int NBARS = 2 * RS + 2 * AS + 2 * BS + 8 + 1 + 2;
+  static constexpr int NBARS = 2 * RS + 2 * AS + 2 * BS + 16 + 1 + 2;
   static constexpr int SMEM = BAR_OFF + NBARS * 8 + 16 + 1024;  // + slack for 1 KB alignment
-  static constexpr int TMEM_COLS = 4 * BN;
   static_assert(RAW_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
   static_assert(SC_BYTES % 16 == 0, "align");
 };
@@ -91,10 +102,10 @@ struct Bars {
   __device__ uint32_t b_full(int i) const { return base + 8 * (2 * RS + 2 * AS + i); }
   __device__ uint32_t b_empty(int i) const { return base + 8 * (2 * RS + 2 * AS + BS + i); }
   __device__ uint32_t acc_full(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + i); }
-  __device__ uint32_t acc_empty(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 4 + i); }
-  __device__ uint32_t done() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 8); }
-  __device__ uint32_t min_full() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 9); }
-  __device__ uint32_t min_empty() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 10); }
+  __device__ uint32_t acc_empty(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 8 + i); }
+  __device__ uint32_t done() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 16); }
+  __device__ uint32_t min_full() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 17); }
+  __device__ uint32_t min_empty() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 18); }
 };
 
 // Wait used while draining: ignores the abort flag, gives up at `deadline`.
@@ -199,7 +210,7 @@ __device__ __forceinline__ void unpack_q6k_stage(const uint8_t* row_window, int 
 
 // --------------------------------------------------------------- kernel --
 template <int QT, int BN, bool DOTS>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const float* __restrict__ scl, const uint8_t* __restrict__ W, float* __restrict__ out,
                    int32_t* __restrict__ dots, int od, int K, int nt, int ntp, int* status, int limit_ms,
@@ -226,17 +237,17 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::RS; ++i) {
       mbar_init(bars.raw_full(i), 1);
-      mbar_init(bars.raw_empty(i), C::MINMMA && !DOTS ? 3 : 2);  // unpack warps (+ the min-term MMAs)
+      mbar_init(bars.raw_empty(i), C::NU + (C::MINMMA && !DOTS ? 1 : 0));  // unpack warps (+ the min-term MMAs)
     }
     for (int i = 0; i < C::AS; ++i) {
-      mbar_init(bars.a_full(i), 2);
+      mbar_init(bars.a_full(i), C::NU);
       mbar_init(bars.a_empty(i), 1);
     }
     for (int i = 0; i < C::BS; ++i) {
       mbar_init(bars.b_full(i), 1);
       mbar_init(bars.b_empty(i), 1 + 8);
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < C::NBUF; ++i) {
       mbar_init(bars.acc_full(i), 1);
       mbar_init(bars.acc_empty(i), 8);
     }
@@ -363,9 +374,9 @@ __global__ void __launch_bounds__(384, 1)
       tc_commit(bars.done());
       drain_wait(bars.done(), 0, global_ns() + 1000000000ull);
     }
-  } else if (warp < 4) {
+  } else if (warp < C::EPI0) {
     // ----------------------------------------------------------- unpack
-    const int ut = threadIdx.x - 64;  // 0..63; rows ut and ut + 64
+    const int ut = threadIdx.x - 64;  // rows ut + 32 * NU * rr, rr < UROWS
     bool ok = true;
     for (int b = 0; b < nsb && ok; ++b) {
       const int rs = b % C::RS;
@@ -382,8 +393,8 @@ __global__ void __launch_bounds__(384, 1)
           // m[r][j] of the 8 sub-blocks as bf16 (exact small integers), the
           // same 16 bytes for parts 0, 1, 2, zeros for the fourth chunk
 #pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const int r = ut + 64 * rr;
+          for (int rr = 0; rr < C::UROWS; ++rr) {
+            const int r = ut + 32 * C::NU * rr;
             const uint4 hdr = *reinterpret_cast<const uint4*>(raw + r * C::RAW_ROW);
             uint32_t mw[4];
 #pragma unroll
@@ -401,8 +412,8 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int r = ut + 64 * rr;
+        for (int rr = 0; rr < C::UROWS; ++rr) {
+          const int r = ut + 32 * C::NU * rr;
           if (QT == kQ4)
             unpack_q4k_pair<!DOTS>(raw + r * C::RAW_ROW, s, a + r * 16);
           else
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(384, 1)
   } else {
     // --------------------------------------------------------- epilogue
     const int q = warp & 3;               // TMEM lane quarter this warp may read
-    const int hc = (warp - 4) >> 2;       // column half
+    const int hc = (warp - C::EPI0) >> 2;  // column half
     const int r = 32 * q + lane;          // tile row
     const int row_g = row0 + r;
     const bool row_ok = row_g < od;
@@ -428,9 +439,17 @@ __global__ void __launch_bounds__(384, 1)
     constexpr int CH = HALF / 32;
     const size_t row_bytes = (size_t)nsb_all * (QT == kQ4 ? kQ4KBytes : kQ6KBytes);
     const uint8_t* wrow = W + (size_t)row_c * row_bytes;
-    float acc[HALF];
+    // Q4_K: one f32 per token of the warp's columns (one FMA per output and
+    // group, measured faster than packed pairs); Q6_K: packed pairs of tokens
+    // (2i, 2i + 1), so the group's scale multiply and the FMA take one
+    // instruction per two outputs each
+    constexpr bool PK = QT != kQ4;
+    float acc[PK ? 1 : HALF];
+    f2 acc2[PK ? HALF / 2 : 1];
 #pragma unroll
-    for (int i = 0; i < HALF; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < (PK ? 1 : HALF); ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < (PK ? HALF / 2 : 1); ++i) acc2[i] = 0ull;
     float sigma = 1.0f;  // acc holds (partial sum) / sigma
     int u = 0;
     bool ok = true;
@@ -464,8 +483,14 @@ __global__ void __launch_bounds__(384, 1)
           const float ratio = sigma * __fdividef(1.0f, d);
           sigma = d;
           if (b > 0) {
+            if constexpr (PK) {
+              const f2 r2 = pk2(ratio, ratio);
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) acc[i] *= ratio;
+              for (int i = 0; i < HALF / 2; ++i) acc2[i] = mul2(acc2[i], r2);
+            } else {
+#pragma unroll
+              for (int i = 0; i < HALF; ++i) acc[i] *= ratio;
+            }
           }
         }
         if (QT == kQ4) {
@@ -499,12 +524,12 @@ __global__ void __launch_bounds__(384, 1)
           const int sub = QT == kQ4 ? gi : (gi >> 1);  // 32-value sub-block within the stage
           const float* sg = scp + sub * BN + hc * HALF;  // dx of this group's tokens
           const float coef = DOTS || QT == kQ4 ? 1.0f : gcoef[4 * s + gi];
+          const f2 coef2 = pk2(coef, coef);
 #pragma unroll
           for (int c = 0; c < CH; ++c) {
             uint32_t P[32];
             __syncwarp();
-            tc_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + hc * HALF + 32 * c), P);
-            tc_wait_ld(P);
+            tc_ld_32x32_sync(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + hc * HALF + 32 * c), P);
             if (DOTS) {
               const int ng = QT == kQ4 ? (K >> 5) : (K >> 4);
               const int grp = QT == kQ4 ? 8 * (b + b_off) + 2 * s + gi : 16 * (b + b_off) + 4 * s + gi;
@@ -518,10 +543,19 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
               for (int i = 0; i < 32; i += 4) {
                 const float4 v = *reinterpret_cast<const float4*>(sg + 32 * c + i);
-                const float dx[4] = {v.x * coef, v.y * coef, v.z * coef, v.w * coef};
+                if constexpr (PK) {  // Q6_K: dx times the group's scale, then the FMA
+                  const f2 dx01 = mul2(pk2(v.x, v.y), coef2), dx23 = mul2(pk2(v.z, v.w), coef2);
+                  f2& a01 = acc2[(32 * c + i) / 2];
+                  f2& a23 = acc2[(32 * c + i) / 2 + 1];
+                  a01 = fma2(dx01, pk2(__uint_as_float(P[i]), __uint_as_float(P[i + 1])), a01);
+                  a23 = fma2(dx23, pk2(__uint_as_float(P[i + 2]), __uint_as_float(P[i + 3])), a23);
+                } else {  // Q4_K: the group's scale is folded into the weight operand
+                  static_assert(QT == kQ4, "the scalar form has no group scale");
+                  const float dx[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  acc[32 * c + i + e] = fmaf(dx[e], __uint_as_float(P[i + e]), acc[32 * c + i + e]);
+                  for (int e = 0; e < 4; ++e)
+                    acc[32 * c + i + e] = fmaf(dx[e], __uint_as_float(P[i + e]), acc[32 * c + i + e]);
+                }
               }
             }
           }
@@ -546,8 +580,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < CH; ++c) {
           uint32_t Q[32];
           __syncwarp();
-          tc_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::NBUF * BN + hc * HALF + 32 * c), Q);
-          tc_wait_ld(Q);
+          tc_ld_32x32_sync(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::NBUF * BN + hc * HALF + 32 * c), Q);
 #pragma unroll
           for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(mc, __uint_as_float(Q[i]), acc[32 * c + i]);
         }
@@ -559,9 +592,11 @@ __global__ void __launch_bounds__(384, 1)
     }
     if (!DOTS && ok && row_ok) {
 #pragma unroll
-      for (int i = 0; i < HALF; ++i) {
-        const int t = tok0 + hc * HALF + i;
-        if (t < nt) out[((size_t)blockIdx.z * nt + t) * od + row_g] = sigma * acc[i];  // slice z's partials
+      for (int i = 0; i < HALF; i += 2) {
+        const float2 a = PK ? upk2(acc2[i / 2]) : make_float2(acc[i], acc[i + 1]);
+        const int t = tok0 + hc * HALF + i;  // slice z's partials
+        if (t < nt) out[((size_t)blockIdx.z * nt + t) * od + row_g] = sigma * a.x;
+        if (t + 1 < nt) out[((size_t)blockIdx.z * nt + t + 1) * od + row_g] = sigma * a.y;
       }
     }
   }
@@ -628,7 +663,7 @@ int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, in
   if (S > 1 && !part) return QMM_EWORKSPACE;
   const dim3 grid((unsigned)((od + C::BM - 1) / C::BM), (unsigned)((nt + BN - 1) / BN), (unsigned)S);
   const int limit_ms = stall_ms > 0 ? stall_ms : 4000;
-  gemm_tc_kernel<QT, BN, DOTS><<<grid, 384, C::SMEM, stream>>>(
+  gemm_tc_kernel<QT, BN, DOTS><<<grid, C::THREADS, C::SMEM, stream>>>(
       mw, mx, scl, static_cast<const uint8_t*>(W), S > 1 ? part : out, dots,
       (int)od, (int)K, (int)nt, (int)gemm_ntp(nt), status, limit_ms, stall_ms > 0 ? 1 : 0);
   if (cudaGetLastError() != cudaSuccess) return QMM_ELAUNCH;

@@ -276,13 +276,15 @@ def test_repeated_calls_are_bitwise_deterministic():
         assert_close_rows(o, ora().matmul(c.qtype, W, x, c.od, nthreads=threads()), c.name)
 
 
-@pytest.mark.parametrize("qtype,nt", [(Q6_K, 32), (Q6_K, 64), (Q4_K, 64), (Q4_K, 256)])
-def test_gemm_repeats_bitwise(qtype, nt):
+@pytest.mark.parametrize("qtype,od,nt", [(Q6_K, 4096, 32), (Q6_K, 4096, 64), (Q6_K, 32000, 64), (Q4_K, 4096, 64),
+                                         (Q4_K, 4096, 256), (Q4_K, 14336, 512)])
+def test_gemm_repeats_bitwise(qtype, od, nt):
     """100 back-to-back tensor-core GEMMs of one problem are bit-identical: the
     TMEM accumulators are never overwritten before the epilogue has used them
-    (an early hand-back showed up as rare wrong sums at 32- and 64-token
-    tiles)."""
-    c = synth.Case(qtype, 4096, 4096, nt)
+    and no role reads a stage that is being refilled (races of that kind
+    showed up as a few wrong sums in one warp's block of rows and tokens, most
+    often on the 32000-row Q6_K LM head)."""
+    c = synth.Case(qtype, od, 4096, nt)
     Wd, xd = (dev(a, torch) for a in c.generate())
     ws = qmm.workspace(qmm.qmm_matmul_workspace_bytes(qtype, c.od, c.K, nt), Wd.device)
     first = qmm.matmul(qtype, Wd, xd, c.od, ws=ws)
