@@ -272,6 +272,18 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Hand a shared-memory stage that this warp has READ back to a producer that
+// refills it with TMA / bulk copies.  Those writes go through the async
+// proxy, so the warp's generic-proxy reads are fenced against them first:
+// without the fence a refill can land before the last reads are performed
+// (seen as a few wrong values in the tail of a warp's reads when the
+// producer runs right behind the consumers).  Whole warp; lane 0 arrives.
+__device__ __forceinline__ void release_stage(uint32_t empty_bar) {
+  fence_proxy_async();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar);
+}
+
 // ------------------------------------------------------------ tcgen05 ----
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

@@ -132,11 +132,19 @@ __device__ __forceinline__ uint32_t magic_pair(uint32_t two_codes, uint32_t mask
 // k order: the low nibbles are k 0..31 (sub-block 2p), the high ones k 32..63
 // (sub-block 2p+1).  Each value is sc*nibble (FOLD) or the nibble itself.
 // Output: row-major 8-k chunks at dst + kc*2048 (kc = k/8), 16 bytes each.
+// The 12 words of pair p of one row: the 16-byte header, then qs bytes
+// 32p..32p+31.
+struct Q4Raw {
+  uint4 hdr, q0, q1;
+};
+__device__ __forceinline__ Q4Raw load_q4k_pair(const uint8_t* raw_row, int p) {
+  return {*reinterpret_cast<const uint4*>(raw_row), *reinterpret_cast<const uint4*>(raw_row + 16 + 32 * p),
+          *reinterpret_cast<const uint4*>(raw_row + 16 + 32 * p + 16)};
+}
+
 template <bool FOLD>
-__device__ __forceinline__ void unpack_q4k_pair(const uint8_t* raw_row, int p, uint8_t* dst) {
-  const uint4 hdr = *reinterpret_cast<const uint4*>(raw_row);
-  const uint4 q0 = *reinterpret_cast<const uint4*>(raw_row + 16 + 32 * p);
-  const uint4 q1 = *reinterpret_cast<const uint4*>(raw_row + 16 + 32 * p + 16);
+__device__ __forceinline__ void unpack_q4k_pair(const Q4Raw& rw, int p, uint8_t* dst) {
+  const uint4 hdr = rw.hdr, q0 = rw.q0, q1 = rw.q1;
   const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
   uint32_t mul_lo, off_lo, mul_hi, off_hi;
   if (FOLD) {
@@ -177,11 +185,18 @@ __device__ __forceinline__ void unpack_q4k_pair(const uint8_t* raw_row, int p, u
 // for quads 0-1, the high one for quads 2-3 -- and its top 2 bits from bits
 // 2*quad..2*quad+1 of qh[32n + l].  Stage s covers half n = s/2, quads
 // 2(s%2) and 2(s%2)+1.
-__device__ __forceinline__ void unpack_q6k_stage(const uint8_t* row_window, int blk_off, int s, uint8_t* dst) {
+struct Q6Raw {
+  uint32_t L[16], H[8];  // ql bytes 64n..64n+63, qh bytes 32n..32n+31 of half n = s/2
+};
+__device__ __forceinline__ void load_q6k_stage(const uint8_t* row_window, int blk_off, int s, Q6Raw& rw) {
   const int n = s >> 1;
-  uint32_t L[16], H[8];
-  load_words_even<16>(row_window, blk_off + 64 * n, L);
-  load_words_even<8>(row_window, blk_off + 128 + 32 * n, H);
+  load_words_even<16>(row_window, blk_off + 64 * n, rw.L);
+  load_words_even<8>(row_window, blk_off + 128 + 32 * n, rw.H);
+}
+
+__device__ __forceinline__ void unpack_q6k_stage(const Q6Raw& rw, int s, uint8_t* dst) {
+  const uint32_t* L = rw.L;
+  const uint32_t* H = rw.H;
   const bool upper = s & 1;
   const uint32_t mul = 0x3C003C00u, off = 0xE420E420u;  // 1.0, -1056.0 (= -1024 - 32)
 #pragma unroll
@@ -411,21 +426,30 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
             *reinterpret_cast<uint4*>(am + 6144) = make_uint4(0, 0, 0, 0);
           }
         }
+        // all rows' raw words first, then the conversions and stores: the
+        // compiler cannot move a later row's loads above an earlier row's
+        // stores (both are shared memory), so this overlaps their latency
+        if constexpr (QT == kQ4) {
+          Q4Raw rw[C::UROWS];
 #pragma unroll
-        for (int rr = 0; rr < C::UROWS; ++rr) {
-          const int r = ut + 32 * C::NU * rr;
-          if (QT == kQ4)
-            unpack_q4k_pair<!DOTS>(raw + r * C::RAW_ROW, s, a + r * 16);
-          else
-            unpack_q6k_stage(raw + r * C::RAW_ROW, ((b + b_off) * kQ6KBytes) & 15, s, a + r * 16);
+          for (int rr = 0; rr < C::UROWS; ++rr) rw[rr] = load_q4k_pair(raw + (ut + 32 * C::NU * rr) * C::RAW_ROW, s);
+#pragma unroll
+          for (int rr = 0; rr < C::UROWS; ++rr) unpack_q4k_pair<!DOTS>(rw[rr], s, a + (ut + 32 * C::NU * rr) * 16);
+        } else {
+          const int blk_off = ((b + b_off) * kQ6KBytes) & 15;
+          Q6Raw rw[C::UROWS];
+#pragma unroll
+          for (int rr = 0; rr < C::UROWS; ++rr)
+            load_q6k_stage(raw + (ut + 32 * C::NU * rr) * C::RAW_ROW, blk_off, s, rw[rr]);
+#pragma unroll
+          for (int rr = 0; rr < C::UROWS; ++rr) unpack_q6k_stage(rw[rr], s, a + (ut + 32 * C::NU * rr) * 16);
         }
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.a_full(as));
       }
       if (!ok) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.raw_empty(rs));
+      release_stage(bars.raw_empty(rs));
     }
   } else {
     // --------------------------------------------------------- epilogue
@@ -565,8 +589,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
           if (lane == 0) mbar_arrive(bars.acc_empty(buf));
         }
         if (!ok) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.b_empty(bs));
+        release_stage(bars.b_empty(bs));  // the stage's dx rows were read
       }
       if (MIN && ok) {
         // the super-block's min term: acc += (-dmin / sigma) * D_min

@@ -453,8 +453,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         }
       }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      release_stage(empty0 + 8 * st);
       if (!DOTS && seg == nseg - 1) {
         // reduce the R x NT partial sums over the warp; lane i*NT+t stores (row i, token t)
         float mine = 0.0f;

@@ -415,8 +415,7 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    release_stage(empty0 + 8 * st);
 
     int fresh = -1;
     if (!DOTS && seg == nseg - 1) {
