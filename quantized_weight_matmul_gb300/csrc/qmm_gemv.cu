@@ -315,6 +315,8 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         c_lo[i] = dmin * (float)(m2 & 0xFFu);
         c_hi[i] = dmin * (float)(m2 >> 8);
       }
+      // the stage's words are in registers: hand it back before the dots
+      release_stage(empty0 + 8 * st);
       if (live) {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -396,6 +398,8 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) scl[i][j] = d * (float)(int8_t)((sw[0] >> (8 * j)) & 0xFFu);
       }
+      // the stage's words are in registers: hand it back before the dots
+      release_stage(empty0 + 8 * st);
       if (live) {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -453,7 +457,6 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         }
       }
       }
-      release_stage(empty0 + 8 * st);
       if (!DOTS && seg == nseg - 1) {
         // reduce the R x NT partial sums over the warp; lane i*NT+t stores (row i, token t)
         float mine = 0.0f;
