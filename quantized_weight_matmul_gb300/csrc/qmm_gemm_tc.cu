@@ -30,8 +30,10 @@
 //               register accumulators, one fp32 store at the end.  A TMEM
 //               accumulator is handed back to the MMA thread only after the
 //               epilogue has finished the arithmetic on the values it read
-//               from it; releasing it right after tcgen05.wait::ld produced
-//               rare wrong sums in stress runs, holding it does not.
+//               from it.
+// Stages that a role reads with ordinary loads and the producer refills with
+// TMA (raw weights, the per-token scale rows) are handed back through
+// release_stage, which fences the reads against the async-proxy refill.
 // Every wait is bounded: a wait that runs past its deadline raises the CTA's
 // abort flag and QMM_ETIMEOUT in the status word, all roles leave their
 // loops, in-flight copies and MMAs are drained, and TMEM is freed.
