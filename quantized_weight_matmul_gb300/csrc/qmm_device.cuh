@@ -23,22 +23,12 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
   return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xFFFFu)));
 }
 
-// The 6-bit (scale, min) pair of Q4_K sub-block j from the 12 packed bytes
-// ("llama.cpp MMQ", sec. 6, get_scale_min_k4): sub-blocks 0-3 keep both in the
-// low 6 bits of bytes j and j+4; sub-blocks 4-7 keep the low 4 bits in the two
-// nibbles of byte j+4 and the top 2 bits in the top of bytes j-4 and j.
-__device__ __forceinline__ void q4k_scale_min(const uint8_t* s, int j, int& sc, int& m) {
-  if (j < 4) {
-    sc = s[j] & 63;
-    m = s[j + 4] & 63;
-  } else {
-    sc = (s[j + 4] & 0x0F) | ((s[j - 4] >> 6) << 4);
-    m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
-  }
-}
-
-// Same unpack from the three header words that hold scales[0..11] (words 1..3
-// of the 16-byte Q4_K header: bytes 4..15 of the block).
+// The 6-bit (scale, min) pair of Q4_K sub-block j ("llama.cpp MMQ", sec. 6,
+// get_scale_min_k4) from the three header words that hold scales[0..11]
+// (words 1..3 of the 16-byte Q4_K header: bytes 4..15 of the block):
+// sub-blocks 0-3 keep both in the low 6 bits of bytes j and j+4; sub-blocks
+// 4-7 keep the low 4 bits in the two nibbles of byte j+4 and the top 2 bits
+// in the top of bytes j-4 and j.
 __device__ __forceinline__ void q4k_scale_min_words(uint32_t w0, uint32_t w1, uint32_t w2, int j,
                                                     int& sc, int& m) {
   // byte k of scales[] = byte (k%4) of word (k/4)

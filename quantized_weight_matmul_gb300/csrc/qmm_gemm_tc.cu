@@ -705,9 +705,15 @@ int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, in
 template <int QT, bool DOTS>
 int launch_qt(const void* W, const __half* xh, const float* scl, float* out, int32_t* dots, float* part, int64_t od,
               int64_t K, int64_t nt, int* status, int stall_ms, cudaStream_t stream) {
-  if (DOTS || nt > 64)
-    return launch_cfg<QT, 128, DOTS>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
-  return launch_cfg<QT, 64, DOTS>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
+  // the block-dot hook always takes the 128-token tile, so only the product
+  // path instantiates the 64-token one
+  if constexpr (DOTS) {
+    return launch_cfg<QT, 128, true>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
+  } else {
+    if (nt > 64)
+      return launch_cfg<QT, 128, false>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
+    return launch_cfg<QT, 64, false>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
+  }
 }
 
 }  // namespace
