@@ -83,8 +83,8 @@ size_t qmm_xds_bytes(int64_t nt, int64_t K);
  * 0 for invalid input. */
 size_t qmm_gemm_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
 
-/* Workspace qmm_matmul needs: 0 on its MMVQ routes (nt <= 8), else
- * qmm_gemm_workspace_bytes. */
+/* Workspace qmm_matmul needs: 0 on its MMVQ routes (at most 16 tokens; see
+ * qmm_matmul and qmm_matmul_path), else qmm_gemm_workspace_bytes. */
 size_t qmm_matmul_workspace_bytes(int qtype, int64_t od, int64_t K, int64_t nt);
 
 /* Routes of qmm_matmul (see there), as returned by qmm_matmul_path. */
