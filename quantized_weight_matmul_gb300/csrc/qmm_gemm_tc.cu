@@ -16,7 +16,7 @@
 //
 // One CTA computes a 128-row x BN-token tile with 12 warps:
 //   warp 0      TMA producer: raw weight super-blocks (128 rows x 144 B, or
-//               224 B windows for the 2-byte-aligned Q6_K blocks), the f16
+//               240 B windows for the 2-byte-aligned Q6_K blocks), the f16
 //               activation tile (BN x 64, 128-byte swizzle) and the
 //               token-contiguous (dx, s) rows of the same 64 k.
 //   warp 1      TMEM allocation and the single MMA-issuing thread: per scale
@@ -63,7 +63,10 @@ struct Cfg {
   static constexpr int THREADS = 32 * (EPI0 + 8);
   static constexpr int KS = 64;  // k per operand stage
   static constexpr int RS = 2, AS = 3, BS = 4;
-  static constexpr int RAW_ROW = QT == kQ4 ? 144 : 224;
+  // raw bytes per row and super-block in shared memory (Q6_K: a window
+  // around the 2-byte-aligned 210-byte block; 240 rather than 224 bytes, so
+  // that a warp's 32-bit loads of 32 rows hit 8 bank offsets instead of 4)
+  static constexpr int RAW_ROW = QT == kQ4 ? 144 : 240;
   static constexpr int GPS = QT == kQ4 ? 2 : 4;  // scale groups per stage
   static constexpr int MPG = QT == kQ4 ? 2 : 1;  // K=16 MMAs per group
   static constexpr int RAW_BYTES = BM * RAW_ROW;
