@@ -206,6 +206,39 @@ def test_gemm_matches_oracle(qtype, od, K, nt):
     assert qmm.qmm_sync_status(0) == qmm.QMM_OK
 
 
+@pytest.mark.parametrize("qtype,nt", [(Q4_K, 1), (Q4_K, 8), (Q4_K, 70), (Q6_K, 1), (Q6_K, 8), (Q6_K, 70)])
+def test_degenerate_blocks_match_oracle(qtype, nt):
+    """Degenerate blocks on every route (fused MMVQ at nt = 1, warp-MMA MMVQ at
+    nt = 8, tensor-core GEMM at nt = 70): super-blocks whose scale d is zero
+    (also a row's first one, where the GEMM epilogue has no running scale yet),
+    Q4_K super-blocks with dmin = 0, all-zero blocks, Q6_K group scales 0 and
+    -128, and zero activation blocks and tokens."""
+    od, K = 300, 4096
+    W, x = _case(qtype, od, K, nt, outliers=True, seed=11)
+    nsb, bb = K // 256, (144 if qtype == Q4_K else 210)
+    Wb = W.reshape(od, nsb, bb).copy()
+    r, b = np.meshgrid(np.arange(od), np.arange(nsb), indexing="ij")
+    dpos = slice(0, 2) if qtype == Q4_K else slice(208, 210)
+    Wb[(r + b) % 3 == 0, dpos] = 0                      # d = 0 (b = 0 for every third row)
+    if qtype == Q4_K:
+        Wb[(r + 2 * b) % 5 == 0, 2:4] = 0               # dmin = 0
+    else:
+        Wb[::2, :, 192] = 0                             # group scale 0
+        Wb[::2, :, 193] = 0x80                          # group scale -128
+    Wb[(7 * r + b) % 11 == 0, :] = 0                    # all-zero blocks
+    W = Wb.reshape(od, nsb * bb)
+    x = x.copy()
+    x[:, 96:128] = 0.0                                  # a zero block in every token
+    if nt > 1:
+        x[nt // 2] = 0.0                                # a zero token
+    out = qmm.matmul(qtype, dev(W, torch), dev(x, torch), od).cpu().numpy()
+    ref = ora().matmul(qtype, W, x, od, nthreads=threads())
+    assert_close_rows(out, ref, f"degenerate q{qtype} nt={nt}")
+    if nt > 1:
+        assert not out[nt // 2].any()
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+
+
 def _full_size(case):
     W, x = case.generate()
     Wd, xd = dev(W, torch), dev(x, torch)
