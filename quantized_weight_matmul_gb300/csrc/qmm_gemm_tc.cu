@@ -53,10 +53,10 @@ constexpr int kQ4 = 0, kQ6 = 1;
 template <int QT, int BN>
 struct Cfg {
   static constexpr int BM = 128;
-  // unpack warps.  Four (14 warps) would halve Q6_K's unpack time, but that
-  // layout returned wrong sums in a few per cent of back-to-back Q6_K calls
-  // (one epilogue warp's 32 rows x 4 tokens), with either epilogue form and
-  // either accumulator count; with two every repeat is bit-identical.
+  // unpack warps.  A 14-warp layout with four caps a thread at 128 registers
+  // and was measured no faster for Q6_K (it also exposed, before the stages
+  // were handed back through release_stage, the cross-proxy refill race that
+  // release_stage closes).
   static constexpr int NU = 2;
   static constexpr int UROWS = BM / (32 * NU);  // rows each unpack thread converts per stage
   static constexpr int EPI0 = 2 + NU;           // first of the 8 epilogue warps
