@@ -18,8 +18,7 @@ __device__ int g_status_word;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices] = {};
+PerDevice<int*> g_status_ptr;
 std::atomic<int> g_stall_ms{0};
 
 bool valid_qtype(int q) { return q == QMM_Q4_K || q == QMM_Q6_K; }
@@ -38,26 +37,30 @@ int check_shape(int64_t od, int64_t K, int64_t nt) {
 int status_ptr(int** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMM_EDEVICE;
-  if (!g_status_ptr[dev]) {
+  int* ptr = g_status_ptr.get(dev);
+  if (!ptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return QMM_EDEVICE;
-    g_status_ptr[dev] = static_cast<int*>(p);
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || !p) return QMM_EDEVICE;
+    ptr = static_cast<int*>(p);
+    g_status_ptr.set(dev, ptr);
   }
-  *out = g_status_ptr[dev];
+  *out = ptr;
   return QMM_OK;
 }
 
 int check_device() {
-  static int cached[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
+  static PerDevice<int> cached;  // 0 unknown, 1 ok, -1 unsupported
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMM_EDEVICE;
-  if (cached[dev] == 0) {
+  int v = cached.get(dev);
+  if (v == 0) {
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cached[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    v = (major == 10 && minor == 3) ? 1 : -1;
+    cached.set(dev, v);
   }
-  return cached[dev] == 1 ? QMM_OK : QMM_EDEVICE;
+  return v == 1 ? QMM_OK : QMM_EDEVICE;
 }
 
 // f16 codes, token-contiguous scale rows, then the split-K partial sums
@@ -74,14 +77,24 @@ int matmul_route(int qtype, int64_t nt, int64_t K) {
   return QMM_PATH_MMQ;
 }
 
-int gemm_core(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
-              int64_t od, int64_t K, int64_t nt, void* ws, size_t ws_bytes, bool prep, cudaStream_t st) {
+// Every refusal of the tensor-core route, checked before any device work is
+// enqueued; on success *status is the device status word.
+// The tensor-core route's own shape rule (host only): the Q6_K weight map
+// needs a 16-byte row pitch, which 210-byte blocks give every 8 blocks.
+int gemm_shape(int qtype, int64_t K) { return qtype == QMM_Q6_K && K % 2048 ? QMM_EINVAL_SHAPE : QMM_OK; }
+
+int gemm_check(int qtype, int64_t od, int64_t K, int64_t nt, const void* ws, size_t ws_bytes, int** status) {
   if (ws_bytes < gemm_ws(od, K, nt)) return QMM_EWORKSPACE;
   if (!ws) return QMM_ENULL;
   if (!aligned16(ws)) return QMM_EALIGN;
-  if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
+  if (int rc = gemm_shape(qtype, K)) return rc;
+  return status_ptr(status);
+}
+
+int gemm_core(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
+              int64_t od, int64_t K, int64_t nt, void* ws, size_t ws_bytes, bool prep, cudaStream_t st) {
   int* status = nullptr;
-  int rc = status_ptr(&status);
+  int rc = gemm_check(qtype, od, K, nt, ws, ws_bytes, &status);
   if (rc) return rc;
   __half* xh = static_cast<__half*>(ws);
   float* scl = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + gemm_xh_bytes(nt, K));
@@ -200,10 +213,9 @@ int qmm_matmul(int qtype, const void* W, const float* x, int8_t* xq, float* xds,
     if (rc) return rc;
     return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, status, true, st);
   }
-  if (ws_bytes < gemm_ws(od, K, nt)) return QMM_EWORKSPACE;
-  if (!workspace) return QMM_ENULL;
-  if (!aligned16(workspace)) return QMM_EALIGN;
-  if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
+  int* status = nullptr;
+  rc = gemm_check(qtype, od, K, nt, workspace, ws_bytes, &status);
+  if (rc) return rc;
   // the quantizer writes the tensor-core operands directly: no separate prepass
   __half* xh = static_cast<__half*>(workspace);
   float* scl = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gemm_xh_bytes(nt, K));
@@ -296,17 +308,17 @@ namespace qmm {
 namespace {
 
 static __device__ __align__(256) uint8_t g_builtin_ws[QMM_BUILTIN_WORKSPACE_BYTES];
-void* g_builtin_ws_ptr[kMaxDevices] = {};
+PerDevice<void*> g_builtin_ws_ptr;
 
 int builtin_ws_ptr(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMM_EDEVICE;
-  if (!g_builtin_ws_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_builtin_ws) != cudaSuccess || !p) return QMM_EDEVICE;
-    g_builtin_ws_ptr[dev] = p;
+  void* ptr = g_builtin_ws_ptr.get(dev);
+  if (!ptr) {
+    if (cudaGetSymbolAddress(&ptr, g_builtin_ws) != cudaSuccess || !ptr) return QMM_EDEVICE;
+    g_builtin_ws_ptr.set(dev, ptr);
   }
-  *out = g_builtin_ws_ptr[dev];
+  *out = ptr;
   return QMM_OK;
 }
 
@@ -322,10 +334,17 @@ extern "C" int qmm_gemm_builtin_workspace(int qtype, const void* W, const int8_t
   if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
   const size_t need = gemm_ws(od, K, nt);
   if (need > (size_t)QMM_BUILTIN_WORKSPACE_BYTES) return QMM_EWORKSPACE;
+  rc = gemm_shape(qtype, K);
+  if (rc) return rc;
   rc = check_device();
   if (rc) return rc;
   void* ws = nullptr;
   rc = builtin_ws_ptr(&ws);
+  if (rc) return rc;
+  // every remaining refusal happens here, before the padding clears below
+  // are enqueued: a refused call leaves the shared array untouched
+  int* status = nullptr;
+  rc = gemm_check(qtype, od, K, nt, ws, (size_t)QMM_BUILTIN_WORKSPACE_BYTES, &status);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The prepass writes the scale planes only for tokens < nt; the padding

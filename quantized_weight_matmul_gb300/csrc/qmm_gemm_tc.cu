@@ -671,13 +671,8 @@ int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, in
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (C::SMEM > optin) return QMM_ESMEM;
-  static bool attr_done[64] = {};
-  if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<QT, BN, DOTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
-      return QMM_ESMEM;
-    attr_done[dev] = true;
-  }
+  static PerDevice<bool> attr_done;
+  if (int rc = smem_attr_once(gemm_tc_kernel<QT, BN, DOTS>, C::SMEM, attr_done, dev)) return rc;
   const uint64_t row_bytes = (uint64_t)(K / 256) * (QT == kQ4 ? kQ4KBytes : kQ6KBytes);
   CUtensorMap mw, mx;
   if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, (uint64_t)od, row_bytes,

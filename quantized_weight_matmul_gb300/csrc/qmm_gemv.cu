@@ -509,13 +509,8 @@ int launch_stream(const GemvArgs& a, int stages) {
   const int64_t act_bytes = FUSED ? fused_act_bytes(NT, a.K) : act_bytes_of(NT, a.K);
   const int smem = stages * C::STAGE_BYTES + (int)((act_bytes + 15) & ~15) + 16 * stages + 32 + 1024;
   auto kern = mmvq_stream_kernel<QT, NT, NW, R, DOTS, FUSED>;
-  static bool attr_done[64] = {};
-  if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 8192) !=
-        cudaSuccess)
-      return QMM_ESMEM;
-    attr_done[dev] = true;
-  }
+  static PerDevice<bool> attr_done;
+  if (int rc = smem_attr_once(kern, kSmemBudget + 8192, attr_done, dev)) return rc;
   if (smem > kSmemBudget + 8192) return QMM_ESMEM;
   auto fn = tensor_map_encoder();
   if (!fn) return QMM_ELAUNCH;

@@ -1,6 +1,7 @@
 // qmm_internal.h -- launchers shared between the library's translation units.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <utility>
@@ -12,6 +13,32 @@
 #include "qmm.h"
 
 namespace qmm {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device memo of a set-up step that is idempotent (a kernel's shared-memory
+// attribute, a device symbol's address).  Several host threads may make their
+// first call on a device at the same time: each may then run the step, but the
+// slot is atomic, so a thread that sees it set also sees everything written
+// before it was set.
+template <typename T>
+struct PerDevice {
+  std::atomic<T> slot[kMaxDevices];
+  T get(int dev) const { return slot[dev].load(std::memory_order_acquire); }
+  void set(int dev, T v) { slot[dev].store(v, std::memory_order_release); }
+};
+
+// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes) once per
+// device (dev < kMaxDevices); QMM_ESMEM if the runtime refuses it.
+template <typename Kern>
+int smem_attr_once(Kern kern, int bytes, PerDevice<bool>& done, int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return QMM_EDEVICE;
+  if (done.get(dev)) return QMM_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return QMM_ESMEM;
+  done.set(dev, true);
+  return QMM_OK;
+}
 
 // Layout of the tensor-core GEMM workspace: f16 codes [nt][K]; the scale
 // planes -- the token-contiguous dx rows [K/32][ntp] f32, then for the Q4_K

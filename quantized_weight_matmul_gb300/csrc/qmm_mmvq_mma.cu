@@ -575,12 +575,8 @@ int launch_mma_cfg(const void* W, const int8_t* xq, const float* xds, float* out
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QMM_EDEVICE;
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  static bool attr_done[64] = {};
-  if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
-      return QMM_ESMEM;
-    attr_done[dev] = true;
-  }
+  static PerDevice<bool> attr_done;
+  if (int rc = smem_attr_once(kern, kSmemLimit, attr_done, dev)) return rc;
   // W viewed as [od][row_bytes/8] 8-byte elements; one box = 16 rows x PITCH bytes
   using C = MC<QT>;
   auto fn = tensor_map_encoder();
