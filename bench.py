@@ -10,8 +10,9 @@ projection), through the C ABI.
 value   weight GB/s of the whole job: weight bytes of all steps on all ranks /
         max-over-ranks wall time of the timed region, inputs resident in HBM.
         Each step reads the next of 16 rotating weight copies (557 MB > 4x L2),
-        so no step finds its weights in L2.  The steps are replayed from a
-        CUDA graph of 16 consecutive steps.
+        so no step finds its weights in L2.  The steps are replayed from CUDA
+        graphs of up to 1024 consecutive steps (one graph for K <= 1024),
+        right after the warm-up steps.
 e2e     the same metric with the activations copied from pinned host memory and
         the outputs copied back inside every step, one qmm_matmul call per
         projection; copy-in, matmuls and copy-out are pipelined on three
@@ -21,12 +22,22 @@ roofline  the dominant kernel of the step -- the fused quantize + MMVQ kernel of
         activations read, q8_1 activations and f32 outputs written) per launch
         / its mean launch time (CUDA events around back-to-back launches over
         rotating copies), against the measured HBM copy bandwidth.
+per_nt  the rest of the metric, one record per (shape, nt): Q4_K 4096x4096 and
+        14336x4096 at nt in {1, 2, 4, 8, 16, 128, 512, 2048}, Q6_K 32000x4096 at
+        nt in {1, 8, 32, 64, 80, 256}.  Each case is timed twice from a CUDA
+        graph of back-to-back calls over rotating weight copies (>= 4x L2):
+        the matmul on q8_1 input (us_kernel: qmm_gemv / qmm_gemm, the latter
+        with its operand prepass) and the whole path from f32 activations
+        (us_path: qmm_matmul).  TOPS, weight GB/s and the fractions of the
+        measured HBM copy bandwidth and bf16 tensor peak come from us_kernel.
+roofline_gemm  the prefill GEMM (Q4_K 14336x4096, nt = 512) as its own
+        roofline object: 2*nt*od*K per launch / us_kernel against the measured
+        dense bf16 peak (the tensor-core route issues kind::f16 MMAs).
 cpu_baseline  the CPU oracle (plain scalar C, all host cores) on the same step.
 
 --impl reference   times the CPU oracle alone as the reference arm.
---sweep            one JSON line per case of every workload family: qmm_matmul
-                   (quantize + matmul from f32 activations; --kernel-only: the
-                   matmul kernel on q8_1 input) timings and roofline fractions;
+--sweep            one JSON line per case of every workload family (or of
+                   --shape QTYPE:ODxKxNT[,...]), timed as a per_nt record;
                    not the contract line.
 Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
 torch.distributed.run, one rank per GPU, each rank running the same workload on
@@ -56,6 +67,15 @@ NCOPIES = 16
 # read + write bytes per launch, and the hash of qmm_gemv.cu it was taken on.
 # Reported as roofline.traffic only while the kernel source is unchanged.
 NCU_TRAFFIC = {"source_sha1": "2b6387032060324d16d3758decfceb84e6c26c5e", "bytes_per_launch": 25408256}
+# The same for the tensor-core GEMM (Q4_K 14336 x 4096, nt = 512; prepass and
+# GEMM kernel launches added), keyed on qmm_gemm_tc.cu.
+NCU_TRAFFIC_GEMM = {"source_sha1": None, "bytes_per_launch": None}
+
+# The cases of the per_nt array: (qtype name, od, K, nt values).
+PER_NT = [("Q4_K", 4096, 4096, (1, 2, 4, 8, 16, 128, 512, 2048)),
+          ("Q4_K", 14336, 4096, (1, 2, 4, 8, 16, 128, 512, 2048)),
+          ("Q6_K", 32000, 4096, (1, 8, 32, 64, 80, 256))]
+GEMM_ROOFLINE_CASE = ("Q4_K", 14336, 4096, 512)
 
 
 def log(*a):
@@ -255,6 +275,154 @@ def run_reference(args):
     return 0
 
 
+class GraphSteps:
+    """Replays `n` consecutive steps from at most two CUDA graphs: one of
+    `period` steps and one of the remainder n mod period, so that the calls
+    stay programmatic dependents of each other inside each graph whatever n
+    is.  `capture(m)` returns a graph of m consecutive steps (step k on
+    rotating copy k); by default one of `body(k, stream)` per step."""
+
+    def __init__(self, body, period, stream, capture=None):
+        self.body, self.period, self.stream = body, period, stream
+        self.capture = capture or self._capture_body
+        self.graphs = {}
+
+    def _capture_body(self, n):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            cs = torch.cuda.current_stream().cuda_stream
+            for k in range(n):
+                self.body(k % self.period, cs)
+        return g
+
+
+    def _graph(self, n):
+        if n not in self.graphs:
+            self.graphs[n] = self.capture(n)
+        return self.graphs[n]
+
+    def _chunks(self, n):
+        """Graph sizes run(n) replays: one graph of n steps up to `span`
+        (a multiple of the rotation period), else whole graphs of `span`
+        steps and one of the remainder."""
+        if n <= self.span:
+            return [n] if n else []
+        out = [self.span] * (n // self.span)
+        if n % self.span:
+            out.append(n % self.span)
+        return out
+
+    span = 1024  # steps per graph: graph boundaries break the dependent-launch chain
+
+    def prepare(self, n):
+        """Capture (outside any timed region) the graphs run(n) replays."""
+        for m in set(self._chunks(n)):
+            self._graph(m)
+
+    def run(self, n):
+        for m in self._chunks(n):
+            self.graphs[m].replay()
+
+
+def time_calls(torch, stream, call, ncopy, reps):
+    """Mean µs of one call(k, stream) over `reps` back-to-back calls replayed
+    from one CUDA graph (k cycles over ncopy weight copies), after one
+    untimed replay."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        cs = torch.cuda.current_stream().cuda_stream
+        for k in range(reps):
+            rc = call(k % ncopy, cs)
+            if rc != 0:
+                raise RuntimeError(f"call failed with status {rc}")
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps * 1e3
+
+
+def case_bytes(c, with_f32_x):
+    """Algorithmic HBM bytes of one matmul: weights, q8_1 activations, f32
+    outputs (and the f32 activations the whole path reads)."""
+    return c.weight_bytes + c.nt * c.K * 1.25 + c.nt * c.od * 4 + (c.nt * c.K * 4 if with_f32_x else 0)
+
+
+def measure_case(torch, qmm, synth, c, dev, stream, peaks, l2, min_gpu_ms=25.0):
+    """Both timings of one case (see per_nt in the module docstring)."""
+    W, x = c.generate()
+    ncopy = max(2, min(32, int(4 * l2 // c.weight_bytes) + 1))
+    Ws = [torch.from_numpy(W).to(dev) for _ in range(ncopy)]
+    xd = torch.from_numpy(x).to(dev)
+    with torch.cuda.stream(stream):
+        xq, xds = qmm.quantize_q8_1(xd)
+    xq8 = torch.empty((c.nt, c.K), dtype=torch.int8, device=dev)
+    xds8 = torch.empty((c.nt, c.K // 32, 2), dtype=torch.float32, device=dev)
+    out = torch.empty((c.nt, c.od), dtype=torch.float32, device=dev)
+    route = qmm.qmm_matmul_path(c.qtype, c.od, c.K, c.nt)
+    if route < 0:
+        raise RuntimeError(f"{c.name}: {qmm.qmm_strerror(route)}")
+    use_gemv = route != qmm.QMM_PATH_MMQ
+    need_k = 0 if use_gemv else qmm.qmm_gemm_workspace_bytes(c.qtype, c.od, c.K, c.nt)
+    need_p = qmm.qmm_matmul_workspace_bytes(c.qtype, c.od, c.K, c.nt)
+    ws = qmm.workspace(max(need_k, need_p), dev)
+
+    def kernel(k, s):
+        if use_gemv:
+            return qmm.qmm_gemv(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
+                                c.od, c.K, c.nt, s)
+        return qmm.qmm_gemm(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
+                            c.od, c.K, c.nt, ws.data_ptr(), need_k, s)
+
+    def path(k, s):
+        return qmm.qmm_matmul(c.qtype, Ws[k].data_ptr(), xd.data_ptr(), xq8.data_ptr(), xds8.data_ptr(),
+                              out.data_ptr(), c.od, c.K, c.nt, ws.data_ptr(), need_p,
+                              qmm.QMM_FLAG_STATIC_WEIGHTS, s)
+
+    # a first eager call of each (first-call set-up outside any capture), then
+    # a rough timing to size the graphs
+    with torch.cuda.stream(stream):
+        assert kernel(0, stream.cuda_stream) == 0 and path(0, stream.cuda_stream) == 0
+    torch.cuda.synchronize()
+    est = time_calls(torch, stream, path, ncopy, ncopy)
+    reps = int(max(2 * ncopy, min(4000, min_gpu_ms * 1e3 / max(est, 1e-3))))
+    reps = (reps + ncopy - 1) // ncopy * ncopy
+    us_k = time_calls(torch, stream, kernel, ncopy, reps)
+    us_p = time_calls(torch, stream, path, ncopy, reps)
+    assert qmm.qmm_sync_status(stream.cuda_stream) == qmm.QMM_OK
+    names = {qmm.QMM_PATH_FUSED_MMVQ: "fused quantize+MMVQ (dp4a)", qmm.QMM_PATH_MMVQ: "quantize, MMVQ",
+             qmm.QMM_PATH_MMQ: "quantize, MMQ (tcgen05)"}
+    tops = 2 * c.macs / (us_k / 1e6) / 1e12
+    rec = {"qtype": synth.QTYPE_NAMES[c.qtype], "od": c.od, "K": c.K, "nt": c.nt, "route": names[route],
+           "kernel_calls": "qmm_gemv" if use_gemv else "qmm_gemm (operand prepass + GEMM)",
+           "us_kernel": us_k, "us_path": us_p, "TOPS": tops,
+           "weight_GBs": c.weight_bytes / (us_k / 1e6) / 1e9,
+           "hbm_frac": case_bytes(c, False) / (us_k / 1e6) / 1e9 / peaks["hbm_gbs"],
+           "tensor_frac": None if use_gemv else tops / peaks["bf16_tflops"],
+           "TOPS_path": 2 * c.macs / (us_p / 1e6) / 1e12,
+           "weight_GBs_path": c.weight_bytes / (us_p / 1e6) / 1e9,
+           "hbm_frac_path": case_bytes(c, True) / (us_p / 1e6) / 1e9 / peaks["hbm_gbs"],
+           "copies": ncopy, "reps": reps}
+    del Ws, ws
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_per_nt(torch, qmm, synth, dev, stream, peaks):
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    qt = {"Q4_K": synth.Q4_K, "Q6_K": synth.Q6_K}
+    recs = []
+    for name, od, K, nts in PER_NT:
+        for nt in nts:
+            c = synth.Case(qt[name], od, K, nt, outliers=True)
+            recs.append(measure_case(torch, qmm, synth, c, dev, stream, peaks, l2))
+    return recs
+
+
 def run_gpu(args):
     import torch
     rank, local_rank, world = dist_env()
@@ -292,44 +460,29 @@ def run_gpu(args):
             if rc != qmm.QMM_OK:
                 raise qmm.QmmError(rc, "qmm_matmul")
 
-    # warm up eagerly once (first-call set-up happens outside any capture), then
-    # capture: one graph runs NCOPIES consecutive steps (one per weight copy),
-    # so consecutive matmuls stay programmatic dependents of each other across
-    # steps; single-step graphs cover a remainder of K mod NCOPIES steps
+    # warm up eagerly once (first-call set-up happens outside any capture),
+    # then capture every graph the warm-up and the timed steps replay
     with torch.cuda.stream(stream):
         step(0)
     stream.synchronize()
-
-    def capture(copies):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in copies:
-                step(k, torch.cuda.current_stream().cuda_stream)
-        return g
-
-    g_all = capture(range(NCOPIES))
-    g_one = [capture([k]) for k in range(NCOPIES)]
+    steps_g = GraphSteps(step, NCOPIES, stream)
+    steps_g.prepare(args.warmup)
+    steps_g.prepare(args.steps)
     torch.cuda.synchronize()
     assert qmm.qmm_sync_status(st) == qmm.QMM_OK
 
-    def run_steps(n):
-        for _ in range(n // NCOPIES):
-            g_all.replay()
-        for k in range(n % NCOPIES):
-            g_one[k].replay()
-
-    with torch.cuda.stream(stream):
-        run_steps(args.warmup)
-    torch.cuda.synchronize()
-
-    # ---- timed region: exactly K steps
+    # ---- timed region: exactly K steps.  The clock sampler starts first and
+    # the warm-up steps run right before the timed ones, so that the GPU is
+    # not idle (and its clocks not lowered) when the timed region begins.
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         with torch.cuda.stream(stream):
+            steps_g.run(args.warmup)
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
             ev0.record(stream)
-            run_steps(args.steps)
+            steps_g.run(args.steps)
             ev1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -346,35 +499,16 @@ def run_gpu(args):
     big = max(range(len(cases)), key=lambda i: cases[i].weight_bytes)
     c = cases[big]
     route = routes[big]
-    nrep = 8 * NCOPIES
 
     def kern_run(k, s):
         if route == qmm.QMM_PATH_FUSED_MMVQ:
-            rc = qmm.qmm_matmul(c.qtype, Wcopies[big][k % NCOPIES].data_ptr(), xs[big].data_ptr(),
-                                xqs[big].data_ptr(), xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K,
-                                c.nt, 0, 0, qmm.QMM_FLAG_STATIC_WEIGHTS, s)
-        else:
-            rc = qmm.qmm_gemv(c.qtype, Wcopies[big][k % NCOPIES].data_ptr(), xqs[big].data_ptr(),
-                              xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K, c.nt, s)
-        assert rc == qmm.QMM_OK
+            return qmm.qmm_matmul(c.qtype, Wcopies[big][k].data_ptr(), xs[big].data_ptr(),
+                                  xqs[big].data_ptr(), xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K,
+                                  c.nt, 0, 0, qmm.QMM_FLAG_STATIC_WEIGHTS, s)
+        return qmm.qmm_gemv(c.qtype, Wcopies[big][k].data_ptr(), xqs[big].data_ptr(),
+                            xdss[big].data_ptr(), outs[big].data_ptr(), c.od, c.K, c.nt, s)
 
-    with torch.cuda.stream(stream):
-        kern_run(0, st)
-    stream.synchronize()
-    kg = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(kg, stream=stream):
-        cs = torch.cuda.current_stream().cuda_stream
-        for k in range(nrep):
-            kern_run(k, cs)
-    with torch.cuda.stream(stream):
-        kg.replay()
-        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        k0.record(stream)
-        for _ in range(4):
-            kg.replay()
-        k1.record(stream)
-    torch.cuda.synchronize()
-    kernel_ms = k0.elapsed_time(k1) / (4 * nrep)
+    kernel_us = time_calls(torch, stream, kern_run, NCOPIES, 32 * NCOPIES)
     act_q8 = c.nt * c.K + c.nt * (c.K // 32) * 8  # q8_1 codes + (d, s)
     if route == qmm.QMM_PATH_FUSED_MMVQ:
         # weights + f32 x read + q8_1 written + f32 out written
@@ -383,13 +517,13 @@ def run_gpu(args):
     else:
         alg_bytes = c.weight_bytes + act_q8 + c.nt * c.od * 4
         kname = "mmvq_stream_kernel (MMVQ)"
-    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    achieved = alg_bytes / (kernel_us / 1e6) / 1e9
     traffic = (NCU_TRAFFIC["bytes_per_launch"]
                if NCU_TRAFFIC["source_sha1"] == source_sha1("quantized_weight_matmul_gb300/csrc/qmm_gemv.cu")
                else None)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": kname, "shape": [c.od, c.K], "kernel_us": kernel_ms * 1e3,
+                "kernel": kname, "shape": [c.od, c.K], "kernel_us": kernel_us,
                 "alg_bytes_per_launch": alg_bytes, "peak_source": peaks["source"] + " hbm_gbs (copy)"}
 
     # ---- e2e: host activations in, host outputs back, one C-ABI call per
@@ -399,7 +533,8 @@ def run_gpu(args):
     # serving loop the copies are pipelined with compute on their own streams:
     # activations and outputs are double-buffered on the device, step k's
     # copy-in overlaps step k-1's matmuls and its copy-out step k+1's.  The
-    # steps are replayed from CUDA graphs of 16 steps.
+    # steps are replayed from CUDA graphs of 16 steps (and one of the
+    # remainder).
     nx = [cc.nt * cc.K for cc in cases]
     no = [cc.nt * cc.od for cc in cases]
     x_off = np.cumsum([0] + nx)
@@ -410,7 +545,7 @@ def run_gpu(args):
     od_all = [torch.empty(sum(no), dtype=torch.float32, device=dev) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def e2e_capture(copies):
+    def e2e_capture(n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             cs = torch.cuda.current_stream()
@@ -419,30 +554,31 @@ def run_gpu(args):
             s_in.wait_event(fork)
             s_out.wait_event(fork)
             done, out_done = {}, {}
-            for n, k in enumerate(copies):
-                buf = n % 2
-                if n >= 2:
-                    s_in.wait_event(done[n - 2])  # xd_all[buf] is free again
+            for k in range(n):
+                buf = k % 2
+                if k >= 2:
+                    s_in.wait_event(done[k - 2])  # xd_all[buf] is free again
                 with torch.cuda.stream(s_in):
                     xd_all[buf].copy_(xh_all, non_blocking=True)
                 x_ready = torch.cuda.Event()
                 x_ready.record(s_in)
                 cs.wait_event(x_ready)
-                if n >= 2:
-                    cs.wait_event(out_done[n - 2])  # od_all[buf] has been copied out
+                if k >= 2:
+                    cs.wait_event(out_done[k - 2])  # od_all[buf] has been copied out
                 for i, cc in enumerate(cases):
-                    rc = qmm.qmm_matmul(cc.qtype, Wcopies[i][k].data_ptr(), xd_all[buf][x_off[i]:].data_ptr(),
+                    rc = qmm.qmm_matmul(cc.qtype, Wcopies[i][k % NCOPIES].data_ptr(),
+                                        xd_all[buf][x_off[i]:].data_ptr(),
                                         xqs[i].data_ptr(), xdss[i].data_ptr(), od_all[buf][o_off[i]:].data_ptr(),
                                         cc.od, cc.K, cc.nt, 0, 0, qmm.QMM_FLAG_STATIC_WEIGHTS, cs.cuda_stream)
                     if rc != qmm.QMM_OK:
                         raise qmm.QmmError(rc, "qmm_matmul")
-                done[n] = torch.cuda.Event()
-                done[n].record(cs)
-                s_out.wait_event(done[n])
+                done[k] = torch.cuda.Event()
+                done[k].record(cs)
+                s_out.wait_event(done[k])
                 with torch.cuda.stream(s_out):
                     oh_all[buf].copy_(od_all[buf], non_blocking=True)
-                out_done[n] = torch.cuda.Event()
-                out_done[n].record(s_out)
+                out_done[k] = torch.cuda.Event()
+                out_done[k].record(s_out)
             join_in, join_out = torch.cuda.Event(), torch.cuda.Event()
             join_in.record(s_in)
             join_out.record(s_out)
@@ -450,21 +586,19 @@ def run_gpu(args):
             cs.wait_event(join_out)
         return g
 
-    e_all = e2e_capture(range(NCOPIES))
-    e_one = [e2e_capture([k]) for k in range(NCOPIES)]
     e2e_steps = max(1, min(args.steps, 16000))
+    e2e_g = GraphSteps(None, NCOPIES, stream, capture=e2e_capture)
+    e2e_g.span = 256  # the e2e graphs hold three streams' worth of nodes per step
+    e2e_g.prepare(args.warmup)
+    e2e_g.prepare(e2e_steps)
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            e_one[0].replay()
+        e2e_g.run(args.warmup)
     torch.cuda.synchronize()
     barrier(world)
     with torch.cuda.stream(stream):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(e2e_steps // NCOPIES):
-            e_all.replay()
-        for k in range(e2e_steps % NCOPIES):
-            e_one[k].replay()
+        e2e_g.run(e2e_steps)
         e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -475,8 +609,30 @@ def run_gpu(args):
     e2e = {"value": job_rate(world, wbytes, 1, e2e_ms), "unit": "GB/s",
            "h2d_bytes_per_step": sum(nx) * 4, "d2h_bytes_per_step": sum(no) * 4, "ms_per_step": e2e_ms,
            "steps": e2e_steps, "outputs_copied_back": bool(e2e_ok),
-           "launch": f"CUDA graphs of {NCOPIES} steps; copy-in, matmuls and copy-out on three streams, "
+           "launch": "CUDA graphs of up to 256 steps; copy-in, matmuls and copy-out on three streams, "
                      "double-buffered"}
+    del Wcopies
+    torch.cuda.empty_cache()
+
+    # ---- per_nt: the rest of the metric (rank 0 of each replica set times it
+    # on its own GPU; every rank runs the same kernels, so one suffices)
+    per_nt, roofline_gemm = None, None
+    if rank == 0 and not args.no_per_nt:
+        per_nt = run_per_nt(torch, qmm, synth, dev, stream, peaks)
+        qn, od_, K_, nt_ = GEMM_ROOFLINE_CASE
+        g = next(r for r in per_nt if (r["qtype"], r["od"], r["K"], r["nt"]) == (qn, od_, K_, nt_))
+        flops = 2.0 * nt_ * od_ * K_
+        ach = flops / (g["us_kernel"] / 1e6) / 1e12
+        tr = (NCU_TRAFFIC_GEMM["bytes_per_launch"]
+              if NCU_TRAFFIC_GEMM["source_sha1"] == source_sha1("quantized_weight_matmul_gb300/csrc/qmm_gemm_tc.cu")
+              else None)
+        roofline_gemm = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": ach / peaks["bf16_tflops"], "traffic": tr,
+                         "kernel": "gemm_operand_prep_kernel + gemm_tc_kernel<Q4_K, BN=128> (qmm_gemm)",
+                         "shape": [od_, K_], "nt": nt_, "kernel_us": g["us_kernel"],
+                         "alg_flops_per_launch": flops, "alg_bytes_per_launch": case_bytes(synth.Case(synth.Q4_K, od_, K_, nt_), False),
+                         "peak_source": peaks["source"] + " bf16_tflops (cuBLAS bf16 burst); the MMAs are "
+                                        "kind::f16, whose dense rate equals bf16's"}
 
     # ---- CPU baseline: the oracle on this host's cores (rank 0, N = 1 only)
     cpu = None
@@ -497,9 +653,10 @@ def run_gpu(args):
                        "qtype": "Q4_K", "x": "N(0,1) + 0.1% x20 outliers", "seed": 0,
                        "parallelism": f"replicas x{world}",
                        "l2": f"{NCOPIES} rotating weight copies ({NCOPIES * wbytes / 1e6:.0f} MB > L2)",
-                       "graphs": f"CUDA graph of {NCOPIES} consecutive steps"},
+                       "graphs": "CUDA graphs of up to 1024 consecutive steps"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+            "per_nt": per_nt, "roofline_gemm": roofline_gemm,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -509,8 +666,8 @@ def run_gpu(args):
 
 
 def run_sweep(args):
-    """Timing of every case of every workload family (CUDA graph of back-to-back
-    calls over rotating weight copies)."""
+    """Timing of every case of every workload family (see measure_case); one
+    JSON line per case."""
     import torch
     import quantized_weight_matmul_gb300 as qmm
     from quantized_weight_matmul_gb300 import synth
@@ -518,84 +675,22 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     peaks = load_peaks()
     stream = torch.cuda.Stream(device=dev)
-    st = stream.cuda_stream
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     names = args.families.split(",") if args.families else list(synth.WORKLOADS)
     fams = [(fam, synth.WORKLOADS[fam].cases) for fam in names]
     if args.shape:  # e.g. Q4_K:44032x4096x1 -- one extra case, seeded like the others
-        qt, dims = args.shape.split(":")
-        od_, K_, nt_ = (int(v) for v in dims.split("x"))
-        fams = [("shape", [synth.Case({"Q4_K": synth.Q4_K, "Q6_K": synth.Q6_K}[qt], od_, K_, nt_)])]
+        fams = []
+        for spec in args.shape.split(","):
+            qt, dims = spec.split(":")
+            od_, K_, nt_ = (int(v) for v in dims.split("x"))
+            fams.append(("shape", [synth.Case({"Q4_K": synth.Q4_K, "Q6_K": synth.Q6_K}[qt], od_, K_, nt_)]))
     for fam, fcases in fams:
         for c in fcases:
             if args.case and c.name != args.case:
                 continue
-            W, x = c.generate()
-            ncopy = max(2, min(32, int(4 * l2 // c.weight_bytes) + 1))
-            if args.copies:
-                ncopy = args.copies
-            Ws = [torch.from_numpy(W).to(dev) for _ in range(ncopy)]
-            xd = torch.from_numpy(x).to(dev)
-            xq, xds = qmm.quantize_q8_1(xd)
-            out = torch.empty((c.nt, c.od), dtype=torch.float32, device=dev)
-            route = qmm.qmm_matmul_path(c.qtype, c.od, c.K, c.nt)
-            use_gemv = c.nt <= qmm.qmm_gemv_max_nt() and route != qmm.QMM_PATH_MMQ
-            need = qmm.qmm_gemm_workspace_bytes(c.qtype, c.od, c.K, c.nt)
-            ws = qmm.workspace(need, dev)
-            xq8 = torch.empty((c.nt, c.K), dtype=torch.int8, device=dev)
-            xds8 = torch.empty((c.nt, c.K // 32, 2), dtype=torch.float32, device=dev)
-
-            def launch(k, s=st):
-                if not args.kernel_only:  # the whole path from f32 activations
-                    return qmm.qmm_matmul(c.qtype, Ws[k].data_ptr(), xd.data_ptr(), xq8.data_ptr(),
-                                          xds8.data_ptr(), out.data_ptr(), c.od, c.K, c.nt, ws.data_ptr(), need,
-                                          qmm.QMM_FLAG_STATIC_WEIGHTS, s)
-                if use_gemv:
-                    return qmm.qmm_gemv(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
-                                        c.od, c.K, c.nt, s)
-                return qmm.qmm_gemm(c.qtype, Ws[k].data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(),
-                                    c.od, c.K, c.nt, ws.data_ptr(), need, s)
-
-            reps = args.reps or max(ncopy, int(min(2000, 2e11 / max(c.macs, 1))))
-            with torch.cuda.stream(stream):
-                for k in range(ncopy):
-                    assert launch(k) == 0
-            torch.cuda.synchronize()
-            if args.no_graph:
-                with torch.cuda.stream(stream):
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    for k in range(reps):
-                        launch(k % ncopy)
-                    e1.record(stream)
-            else:
-                gph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gph, stream=stream):
-                    st_cap = torch.cuda.current_stream().cuda_stream
-                    for k in range(reps):
-                        assert launch(k % ncopy, st_cap) == 0
-                with torch.cuda.stream(stream):
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    gph.replay()
-                    e1.record(stream)
-            torch.cuda.synchronize()
-            assert qmm.qmm_sync_status(st) == 0
-            us = e0.elapsed_time(e1) / reps * 1e3
-            # weights + q8_1 activations (+ the f32 activations they come from) + f32 out
-            alg = c.weight_bytes + c.nt * c.K * 1.25 + c.nt * c.od * 4 + (0 if args.kernel_only else c.nt * c.K * 4)
-            tops = 2 * c.macs / (us / 1e6) / 1e12
-            names = {qmm.QMM_PATH_FUSED_MMVQ: "fused quantize+mmvq", qmm.QMM_PATH_MMVQ: "quantize, mmvq",
-                     qmm.QMM_PATH_MMQ: "quantize, mmq-tcgen05"}
-            what = (("mmvq" if use_gemv else "mmq-tcgen05 (with its operand prepass)") if args.kernel_only
-                    else names[route])
-            rec = {"case": c.name, "path": what, "us": us,
-                   "weight_GBs": c.weight_bytes / (us / 1e6) / 1e9, "TOPS": tops,
-                   "hbm_frac": alg / (us / 1e6) / 1e9 / peaks["hbm_gbs"],
-                   "tensor_frac_f16": tops / peaks["bf16_tflops"], "copies": ncopy, "reps": reps}
+            rec = measure_case(torch, qmm, synth, c, dev, stream, peaks, l2)
+            rec["case"] = c.name
             print(json.dumps(rec), flush=True)
-            del Ws, ws
-            torch.cuda.empty_cache()
     return 0
 
 
@@ -609,14 +704,10 @@ def main():
     ap.add_argument("--families", default="")
     ap.add_argument("--case", default="", help="sweep: only the case with this name")
     ap.add_argument("--shape", default="", help="sweep: one case of this shape instead, QTYPE:ODxKxNT")
-    ap.add_argument("--reps", type=int, default=0, help="sweep: timed launches per case")
-    ap.add_argument("--copies", type=int, default=0, help="sweep: rotating weight copies per case")
-    ap.add_argument("--no-graph", action="store_true", help="sweep: launch from Python instead of a CUDA graph")
-    ap.add_argument("--kernel-only", action="store_true",
-                    help="sweep: time qmm_gemv / qmm_gemm on pre-quantized activations instead of qmm_matmul")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-nt", action="store_true", help="leave out the per_nt array and roofline_gemm")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -169,7 +169,9 @@ int qmm_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float
   int* status = nullptr;
   rc = status_ptr(&status);
   if (rc) return rc;
-  return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, status, false,
+  // a programmatic dependent of the preceding kernel: every access that may
+  // depend on it (the weights included) waits for it, the prologue does not
+  return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, status, Dep::kPdl,
                      static_cast<cudaStream_t>(stream));
 }
 
@@ -211,7 +213,7 @@ int qmm_matmul(int qtype, const void* W, const float* x, int8_t* xq, float* xds,
     if (rc) return rc;
     rc = launch_quantize(x, nt, K, xq, xds, nullptr, nullptr, 0, st);
     if (rc) return rc;
-    return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, status, true, st);
+    return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, status, Dep::kPdlStaticW, st);
   }
   int* status = nullptr;
   rc = gemm_check(qtype, od, K, nt, workspace, ws_bytes, &status);
@@ -241,7 +243,7 @@ int qmm_debug_block_dots(int qtype, const void* W, const int8_t* xq, const float
     int* status = nullptr;
     rc = status_ptr(&status);
     if (rc) return rc;
-    return launch_gemv(qtype, W, xq, xds, nullptr, dots, od, K, nt, status, false, st);
+    return launch_gemv(qtype, W, xq, xds, nullptr, dots, od, K, nt, status, Dep::kNone, st);
   }
   if (path == 2) {
     if (nt > kMmaMaxNt) return QMM_EINVAL_SHAPE;
@@ -251,7 +253,7 @@ int qmm_debug_block_dots(int qtype, const void* W, const int8_t* xq, const float
     int* status = nullptr;
     rc = status_ptr(&status);
     if (rc) return rc;
-    return launch_mmvq_mma(qtype, W, xq, xds, nullptr, dots, od, K, nt, status, false, st);
+    return launch_mmvq_mma(qtype, W, xq, xds, nullptr, dots, od, K, nt, status, Dep::kNone, st);
   }
   if (path != 1) return QMM_EINVAL_SHAPE;
   if (!xds) return QMM_ENULL;

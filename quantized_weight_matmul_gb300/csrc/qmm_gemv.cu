@@ -622,17 +622,15 @@ bool gemv_fused_fits(int qtype, int64_t nt, int64_t K) {
 }
 
 int launch_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
-                int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream) {
+                int64_t od, int64_t K, int64_t nt, int* status, Dep dep, cudaStream_t stream) {
   if (qtype != QMM_Q4_K && qtype != QMM_Q6_K) return QMM_EINVAL_QTYPE;
   if (!gemv_type_ok(qtype, K)) return QMM_EINVAL_SHAPE;
   // from a few tokens on the dots run on the warp-level tensor-core MMA
   if (!dots && (nt > 8 || nt >= mma_min_nt(qtype)) && mmvq_mma_fits(qtype, nt, K))
-    return launch_mmvq_mma(qtype, W, xq, xds, out, nullptr, od, K, nt, status, after_quantize, stream);
+    return launch_mmvq_mma(qtype, W, xq, xds, out, nullptr, od, K, nt, status, dep, stream);
   if (!gemv_fits(qtype, nt, K)) return QMM_ESMEM;
-  // right after our quantizer the weight stream may start early: the quantizer
-  // releases its dependents only once everything before it has completed
-  const GemvArgs a{W,    nullptr, const_cast<int8_t*>(xq), const_cast<float*>(xds), out, dots, od, K, status,
-                   after_quantize, after_quantize, stream};
+  const GemvArgs a{W,      nullptr, const_cast<int8_t*>(xq), const_cast<float*>(xds), out, dots, od, K, status,
+                   dep != Dep::kNone, dep == Dep::kPdlStaticW, stream};
   if (qtype == QMM_Q4_K)
     return dots ? launch_staged_nt<kQ4, true>(a, nt) : launch_staged_nt<kQ4, false>(a, nt);
   return dots ? launch_staged_nt<kQ6, true>(a, nt) : launch_staged_nt<kQ6, false>(a, nt);

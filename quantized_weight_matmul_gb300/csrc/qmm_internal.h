@@ -109,25 +109,33 @@ bool gemv_fits(int qtype, int64_t nt, int64_t K);
 // Whether the fused quantize + MMVQ kernel covers nt x K (decode shapes, nt <= 4).
 bool gemv_fused_fits(int qtype, int64_t nt, int64_t K);
 
-// MMVQ (nt <= 8).  dots != nullptr selects the raw block-dot output.  With
-// `after_quantize` the kernel is launched as a programmatic dependent of the
-// quantizer just enqueued (which releases it only once everything before it
-// is complete), so it may start streaming the weights before the activations
-// are ready.
+// How an MMVQ kernel is launched relative to the kernel before it on the
+// stream.
+enum class Dep {
+  kNone,        // an ordinary launch
+  kPdl,         // a programmatic dependent: every global access, the weight
+                // stream included, waits for the preceding grid
+  kPdlStaticW,  // a programmatic dependent whose weight stream may start
+                // before the preceding grid completes (right after our
+                // quantizer, which releases its dependents only once
+                // everything before it is complete)
+};
+
+// MMVQ (nt <= 8).  dots != nullptr selects the raw block-dot output.
 int launch_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
-                int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream);
+                int64_t od, int64_t K, int64_t nt, int* status, Dep dep, cudaStream_t stream);
 
 // Warp-MMA MMVQ (qmm_mmvq_mma.cu) for 1 <= nt <= kMmaMaxNt: whether the
 // activations and a weight ring of at least two stages fit one SM's shared
 // memory (Q6_K also needs K % 2048 == 0), and the launcher.  dots != nullptr
-// selects the raw block-dot output; `after_quantize` as for launch_gemv.
+// selects the raw block-dot output.
 constexpr int kMmaMaxNt = 16;
 // Smallest nt the warp-MMA kernel takes (below it the dp4a MMVQ is faster:
 // its cost per token is small while the MMA's 8-token tile is mostly padding).
 inline int mma_min_nt(int qtype) { return qtype == QMM_Q4_K ? 5 : 2; }
 bool mmvq_mma_fits(int qtype, int64_t nt, int64_t K);
 int launch_mmvq_mma(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
-                    int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream);
+                    int64_t od, int64_t K, int64_t nt, int* status, Dep dep, cudaStream_t stream);
 
 // Fused quantize + MMVQ: x f32 in, q8_1 (xq, xds) and out written.  With
 // `static_w` the weight stream starts before the preceding kernel completes.

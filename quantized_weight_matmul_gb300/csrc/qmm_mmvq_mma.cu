@@ -570,7 +570,8 @@ bool choose_plan(int qt, int ntl, int64_t nt, int64_t K, Plan* out) {
 
 template <int QT, int NTL, bool X16, bool DOTS>
 int launch_mma_cfg(const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots, int64_t od,
-                   int64_t K, int64_t nt, int* status, bool pdl, const Plan& p, cudaStream_t stream) {
+                   int64_t K, int64_t nt, int* status, Dep dep, const Plan& p, cudaStream_t stream) {
+  const bool pdl = dep != Dep::kNone, static_w = dep == Dep::kPdlStaticW;
   auto kern = mmvq_mma_kernel<QT, NTL, X16, DOTS>;
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QMM_EDEVICE;
@@ -595,23 +596,23 @@ int launch_mma_cfg(const void* W, const int8_t* xq, const float* xds, float* out
   int grid = nsm > 0 ? nsm : 152;
   if (grid > tiles) grid = (int)tiles;
   return launch_ex(kern, dim3(grid), dim3(kThreads), (size_t)p.total + 1024, stream, pdl, m, xq, xds, out, dots,
-                   (int)od, (int)K, (int)nt, p.stages, status, pdl ? 1 : 0);
+                   (int)od, (int)K, (int)nt, p.stages, status, static_w ? 1 : 0);
 }
 
 template <int QT, int NTL, bool DOTS>
 int launch_mma_ntl(const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots, int64_t od,
-                   int64_t K, int64_t nt, int* status, bool pdl, cudaStream_t stream) {
+                   int64_t K, int64_t nt, int* status, Dep dep, cudaStream_t stream) {
   Plan p;
   if (!choose_plan(QT, NTL, nt, K, &p)) return QMM_ESMEM;
-  if (p.x16) return launch_mma_cfg<QT, NTL, true, DOTS>(W, xq, xds, out, dots, od, K, nt, status, pdl, p, stream);
-  return launch_mma_cfg<QT, NTL, false, DOTS>(W, xq, xds, out, dots, od, K, nt, status, pdl, p, stream);
+  if (p.x16) return launch_mma_cfg<QT, NTL, true, DOTS>(W, xq, xds, out, dots, od, K, nt, status, dep, p, stream);
+  return launch_mma_cfg<QT, NTL, false, DOTS>(W, xq, xds, out, dots, od, K, nt, status, dep, p, stream);
 }
 
 template <int QT, bool DOTS>
 int launch_mma_qt(const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots, int64_t od,
-                  int64_t K, int64_t nt, int* status, bool pdl, cudaStream_t stream) {
-  if (nt <= 8) return launch_mma_ntl<QT, 1, DOTS>(W, xq, xds, out, dots, od, K, nt, status, pdl, stream);
-  return launch_mma_ntl<QT, 2, DOTS>(W, xq, xds, out, dots, od, K, nt, status, pdl, stream);
+                  int64_t K, int64_t nt, int* status, Dep dep, cudaStream_t stream) {
+  if (nt <= 8) return launch_mma_ntl<QT, 1, DOTS>(W, xq, xds, out, dots, od, K, nt, status, dep, stream);
+  return launch_mma_ntl<QT, 2, DOTS>(W, xq, xds, out, dots, od, K, nt, status, dep, stream);
 }
 
 }  // namespace
@@ -625,13 +626,13 @@ bool mmvq_mma_fits(int qtype, int64_t nt, int64_t K) {
 }
 
 int launch_mmvq_mma(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
-                    int64_t od, int64_t K, int64_t nt, int* status, bool after_quantize, cudaStream_t stream) {
+                    int64_t od, int64_t K, int64_t nt, int* status, Dep dep, cudaStream_t stream) {
   if (!mmvq_mma_fits(qtype, nt, K)) return QMM_ESMEM;
   if (qtype == QMM_Q4_K)
-    return dots ? launch_mma_qt<kQ4, true>(W, xq, xds, out, dots, od, K, nt, status, after_quantize, stream)
-                : launch_mma_qt<kQ4, false>(W, xq, xds, out, dots, od, K, nt, status, after_quantize, stream);
-  return dots ? launch_mma_qt<kQ6, true>(W, xq, xds, out, dots, od, K, nt, status, after_quantize, stream)
-              : launch_mma_qt<kQ6, false>(W, xq, xds, out, dots, od, K, nt, status, after_quantize, stream);
+    return dots ? launch_mma_qt<kQ4, true>(W, xq, xds, out, dots, od, K, nt, status, dep, stream)
+                : launch_mma_qt<kQ4, false>(W, xq, xds, out, dots, od, K, nt, status, dep, stream);
+  return dots ? launch_mma_qt<kQ6, true>(W, xq, xds, out, dots, od, K, nt, status, dep, stream)
+              : launch_mma_qt<kQ6, false>(W, xq, xds, out, dots, od, K, nt, status, dep, stream);
 }
 
 }  // namespace qmm
