@@ -316,9 +316,15 @@ class GraphSteps:
     span = 1024  # steps per graph: graph boundaries break the dependent-launch chain
 
     def prepare(self, n):
-        """Capture (outside any timed region) the graphs run(n) replays."""
+        """Capture the graphs run(n) replays, and replay each new one once,
+        outside any timed region: a graph's first launch also uploads it."""
+        import torch
         for m in set(self._chunks(n)):
-            self._graph(m)
+            if m not in self.graphs:
+                g = self._graph(m)
+                with torch.cuda.stream(self.stream):
+                    g.replay()
+        torch.cuda.synchronize()
 
     def run(self, n):
         for m in self._chunks(n):

@@ -73,7 +73,11 @@ enum {
  * (Q6_K) ([MMQ] sec. 4).  0 for an invalid qtype or shape.  Host only. */
 size_t qmm_weight_bytes(int qtype, int64_t od, int64_t K);
 
-/* Bytes of the q8_1 activations: xq = nt*K int8, xds = nt*(K/32)*2 f32. */
+/* Bytes of the q8_1 activations: xq = nt*K int8, xds = nt*(K/32)*2 f32.
+ * qmm_q8_1_bytes is the size of the codes, nt*K (the same as qmm_xq_bytes);
+ * the (d, s) pairs take qmm_xds_bytes.  0 for a negative size (xds: or a K
+ * that is not a multiple of 32). */
+size_t qmm_q8_1_bytes(int64_t nt, int64_t K);
 size_t qmm_xq_bytes(int64_t nt, int64_t K);
 size_t qmm_xds_bytes(int64_t nt, int64_t K);
 
@@ -137,10 +141,12 @@ int qmm_gemv(int qtype, const void *W, const int8_t *xq, const float *xds, float
 /*
  * MMQ: matmul for any nt >= 1 on the tcgen05 tensor cores ([MMQ] sec. 2-6;
  * [MOJO] "One mma per scale group").  Raw super-blocks are staged into
- * shared memory by TMA, their nibbles (or 6-bit Q6_K codes minus 32) are
- * unpacked in registers into exact small-integer f16 operands, one MMA chain
- * per scale group accumulates the exact integer dot in TMEM (fp32, exact for
- * these magnitudes), and the fp32 epilogue applies d, sc, dx, dmin, m and s.
+ * shared memory by TMA and unpacked in registers into exact small-integer
+ * f16 weight operands that carry the integer group scale (Q4_K sc*nibble;
+ * Q6_K sc*(q - 32), split exactly into two operands), written into tensor
+ * memory; one MMA chain per 32-value block accumulates the exact integer sum
+ * in TMEM (fp32, exact for these magnitudes), and the fp32 epilogue applies
+ * d, dx and, for Q4_K, the min term dmin * sum(m*s).
  * `workspace` (device, 16-byte aligned, >= qmm_gemm_workspace_bytes) holds
  * an f16 copy of xq and the scale planes written by a prepass on `stream`;
  * its contents need not be preserved between calls.  out is overwritten.
@@ -215,11 +221,19 @@ int qmm_matmul(int qtype, const void *W, const float *x, int8_t *xq, float *xds,
  *   Q4_K: dots[t][r][j] = sum_{i<32} nibble[r][32j+i] * xq[t][32j+i], j < K/32
  *   Q6_K: dots[t][r][g] = sum_{i<16} (q6[r][16g+i] - 32) * xq[t][16g+i], g < K/16
  * path 0: the dp4a MMVQ dot code, nt <= 8 (Q6_K: K % 2048 == 0).
- * path 1: the tensor-core (qmm_gemm) dot code; needs xds (for the prepass)
- *         and a workspace of qmm_gemm_workspace_bytes.
+ * path 1: the tensor-core (qmm_gemm) dot code with the same tile choice and
+ *         weight operands as the product kernel, which carry the integer
+ *         group scales, so the sums come out scaled, one per 32-value block:
+ *           Q4_K: dots[t][r][j] = sc_j * D_j (sc_j the 6-bit scale of
+ *                 sub-block j), j < K/32;
+ *           Q6_K: dots[t][r][b] = sc_2b * D_2b + sc_2b+1 * D_2b+1 (the signed
+ *                 int8 scales of the block's two 16-value groups), b < K/32;
+ *         both 0 for a super-block whose d is 0.  Needs xds (for the
+ *         prepass) and a workspace of qmm_gemm_workspace_bytes.
  * path 2: the warp-MMA MMVQ dot code, nt <= 16 (Q6_K: K % 2048 == 0); needs
  *         xds; QMM_ESMEM where the activations do not fit its shared memory.
- * dots is a device buffer of nt*od*(K/32 or K/16) int32.
+ * dots is a device buffer of nt*od*ng int32: ng = K/32, except K/16 for
+ * Q6_K on paths 0 and 2.
  */
 int qmm_debug_block_dots(int qtype, const void *W, const int8_t *xq, const float *xds,
                          int64_t od, int64_t K, int64_t nt, int32_t *dots, int path,
@@ -233,10 +247,12 @@ int qmm_debug_block_dots(int qtype, const void *W, const int8_t *xq, const float
  */
 int qmm_sync_status(void *stream);
 
-/* Test hook: when `on` is nonzero, the next tensor-core GEMM launches on the
- * current device skip one producer arrival on purpose, so their bounded waits
- * run out and report QMM_ETIMEOUT through qmm_sync_status (no trap, no hang:
- * every wait gives up after about `ms` milliseconds).  Off by default. */
+/* Test hook: while `on` is nonzero, every kernel launch with bounded waits
+ * (the tensor-core GEMM and both MMVQ kernels, fused or not) skips one
+ * producer arrival per CTA on purpose, so that its waits run out and report
+ * QMM_ETIMEOUT through qmm_sync_status (no trap, no hang: every wait gives up
+ * after about `ms` milliseconds, in-flight copies are drained).  Off by
+ * default. */
 int qmm_debug_inject_stall(int on, int ms);
 
 /* Static string for a status code. */

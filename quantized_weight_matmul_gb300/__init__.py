@@ -59,6 +59,7 @@ class QmmError(RuntimeError):
 
 _SIGS = {
     "qmm_weight_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64]),
+    "qmm_q8_1_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "qmm_xq_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "qmm_xds_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "qmm_gemm_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
@@ -130,6 +131,7 @@ def _call(name, *args):
 
 # ------------------------------------------------ C-ABI, same names -------
 def qmm_weight_bytes(qtype, od, K): return _call("qmm_weight_bytes", qtype, od, K)
+def qmm_q8_1_bytes(nt, K): return _call("qmm_q8_1_bytes", nt, K)
 def qmm_xq_bytes(nt, K): return _call("qmm_xq_bytes", nt, K)
 def qmm_xds_bytes(nt, K): return _call("qmm_xds_bytes", nt, K)
 def qmm_gemm_workspace_bytes(qtype, od, K, nt): return _call("qmm_gemm_workspace_bytes", qtype, od, K, nt)
@@ -228,7 +230,7 @@ def matmul(qtype, W, x, od, ws=None, flags=0, return_q8=False):
 def block_dots(qtype, W, xq, xds, od, path):
     torch = _torch()
     nt, K = xq.shape
-    ng = K // (32 if qtype == Q4_K else 16)
+    ng = K // (32 if qtype == Q4_K or path == 1 else 16)
     dots = torch.empty((nt, od, ng), dtype=torch.int32, device=xq.device)
     ws = None
     if path == 1:

@@ -103,10 +103,13 @@ int gemm_core(int qtype, const void* W, const int8_t* xq, const float* xds, floa
     rc = launch_gemm_prep(xq, xds, nt, K, gemm_ntp(nt), xh, scl, st);
     if (rc) return rc;
   }
-  return launch_gemm_tc(qtype, W, xh, scl, out, dots, part, od, K, nt, status, g_stall_ms.load(), st);
+  return launch_gemm_tc(qtype, W, xh, scl, out, dots, part, od, K, nt, status, stall_ms(), st);
 }
 
 }  // namespace
+
+int stall_ms() { return g_stall_ms.load(); }
+
 }  // namespace qmm
 
 using namespace qmm;
@@ -119,6 +122,8 @@ size_t qmm_weight_bytes(int qtype, int64_t od, int64_t K) {
 }
 
 size_t qmm_xq_bytes(int64_t nt, int64_t K) { return nt < 0 || K < 0 ? 0 : (size_t)nt * (size_t)K; }
+
+size_t qmm_q8_1_bytes(int64_t nt, int64_t K) { return qmm_xq_bytes(nt, K); }
 
 size_t qmm_xds_bytes(int64_t nt, int64_t K) {
   return nt < 0 || K < 0 || K % 32 ? 0 : (size_t)nt * (size_t)(K / 32) * 2 * sizeof(float);

@@ -119,6 +119,20 @@ __device__ __forceinline__ f2 mul2(f2 a, f2 b) {
   return d;
 }
 
+// Per-warpgroup register budgets (all four warps of the warpgroup execute
+// it): a warpgroup may give registers back to the block's pool, or take them
+// from it.  The block's pool is what it was launched with (threads x the
+// kernel's register count), so the budgets of all warpgroups must add up to
+// no more than that, or an increase would wait for registers forever.
+template <uint32_t N>
+__device__ __forceinline__ void regs_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_take() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------ timing ----
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -157,6 +171,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// parked by the hardware until it completes (or `ns` nanoseconds pass)
+// instead of returning at once to poll again, which keeps waiting warps off
+// the issue slots and shared-memory ports the working warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, "
+      "p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared abort state of one CTA: a flag every wait polls, the device status
 // word, and the deadline after which a wait gives up.
 struct Guard {
@@ -174,6 +203,20 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Gu
     if (mbar_try_wait(bar, parity)) return true;
     if (*g.abort_flag) return false;
     if ((it & 63u) == 0 && global_ns() > g.deadline_ns) {
+      *g.abort_flag = 1;
+      report(g.status, QMM_ETIMEOUT);
+      return false;
+    }
+  }
+}
+
+// wait_bar whose polls park the thread for up to 20 us each (see
+// mbar_try_wait_sleep); the deadline is checked after every poll.
+__device__ __forceinline__ bool wait_bar_sleep(uint32_t bar, uint32_t parity, const Guard& g) {
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*g.abort_flag) return false;
+    if (global_ns() > g.deadline_ns) {
       *g.abort_flag = 1;
       report(g.status, QMM_ETIMEOUT);
       return false;
@@ -364,6 +407,26 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 // spill one of them in between, which reads it before the data has arrived
 // (wrong values in a few columns of one warp's load, more often under
 // register pressure).  Here the outputs exist only after the wait.
+// 64 columns (two 32-column loads at taddr and taddr + 32) with one wait.
+__device__ __forceinline__ void tc_ld_32x32_x2_sync(uint32_t taddr, uint32_t (&v)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
+        "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]),
+        "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]),
+        "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
+        "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+      : "r"(taddr), "r"(taddr + 32u)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_ld_32x32_sync(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"

@@ -7,36 +7,45 @@
 //   Q6_K: out[t][r] = sum_b sum_g d_b*sc_g*dx_t(g/2)*D_trg,
 //         D = sum over the 16 values of group g of (q6 - 32) * q
 //
-// GB300 design.  The int8 MMA of this part is slow (the legacy warp-level
-// path) and tcgen05 has no int8 kind on sm_103a, so the integer dots run on
-// the f16 kind: every operand is a small integer that f16 holds exactly
-// (nibble*sc <= 945, q6-32 in [-32,31], q8 in [-127,127]) and the f32
-// accumulation of one scale group (|D| < 2^24) is exact, so the TMEM
-// accumulator holds the exact integer dot.
+// GB300 design.  tcgen05 has no int8 kind on sm_103a and the legacy int8
+// warp MMA is slow, so the integer dots run on the f16 kind with operands
+// that are small integers f16 holds exactly; the f32 accumulation of one
+// 32-value block stays below 2^24 in magnitude, so TMEM holds the exact
+// integer sum.  The weight operand carries its integer group scale:
+//   Q4_K  sc_j * nibble (<= 945);
+//   Q6_K  sc_g * (q - 32) split exactly into two operands, hi = sgn*16*(|sc|>>4)
+//         *(q-32) and lo = sgn*(|sc|&15)*(q-32), both dotted with the same
+//         activation codes and accumulated into the same sum, so one
+//         accumulator holds sum_g sc_g*D_g of a whole 32-value block.
+// One accumulator per 32-value block is then rescaled once per output in
+// fp32 by the token's dx (and the row's d, factored out of the running sum).
 //
-// One CTA computes a 128-row x BN-token tile with 12 warps:
+// One CTA computes a 128-row x BN-token tile with 16 warps:
 //   warp 0      TMA producer: raw weight super-blocks (128 rows x 144 B, or
-//               240 B windows for the 2-byte-aligned Q6_K blocks), the f16
-//               activation tile (BN x 64, 128-byte swizzle) and the
-//               token-contiguous (dx, s) rows of the same 64 k.
-//   warp 1      TMEM allocation and the single MMA-issuing thread: per scale
-//               group an MMA chain into one of NBUF TMEM accumulators (3 to 8
-//               of the 512 columns; round robin by group), committed to an
-//               mbarrier.
-//   warps 2-3   unpack: raw nibbles / 6-bit codes -> f16 operand tiles in the
-//               canonical no-swizzle K-major layout (Q4_K folds the 6-bit scale
-//               into the operand: sc*nibble is exact), one 64-k stage at a time.
-//   warps 4-11  epilogue: TMEM -> registers per group, fp32 rescale into
-//               register accumulators, one fp32 store at the end.  A TMEM
-//               accumulator is handed back to the MMA thread only after the
-//               epilogue has finished the arithmetic on the values it read
-//               from it.
+//               240 B windows around the 2-byte-aligned 210-byte Q6_K
+//               blocks), the f16 activation tile (BN x 64 k, 128-byte
+//               swizzle) with the token-contiguous dx rows of the same 64 k,
+//               and for Q4_K the three bf16 parts of s of each super-block.
+//   warp 1      TMEM allocation and the single MMA-issuing thread: per
+//               32-value block an MMA chain into one of NBUF accumulators of
+//               BN columns, committed to an mbarrier; Q4_K's min term
+//               sum_j m_j*s_tj of each super-block is one more entry of the
+//               same accumulator ring (bf16 operands, exact products).
+//   warps 4-7   unpack, one TMEM lane quarter each, one weight row per
+//               thread: raw codes -> the f16 weight operand of a 64-k stage,
+//               written straight into TMEM (tcgen05.st), where the MMA reads
+//               it as its A operand -- the operand never touches shared
+//               memory, whose bandwidth the MMAs' activation reads need.
+//   warps 8-15  epilogue, two per lane quarter (BN/2 token columns each):
+//               per accumulator the TMEM loads of its columns, the
+//               accumulator handed back after the last of them, the fp32
+//               rescale into register accumulators; one store at the end.
 // Stages that a role reads with ordinary loads and the producer refills with
-// TMA (raw weights, the per-token scale rows) are handed back through
-// release_stage, which fences the reads against the async-proxy refill.
-// Every wait is bounded: a wait that runs past its deadline raises the CTA's
-// abort flag and QMM_ETIMEOUT in the status word, all roles leave their
-// loops, in-flight copies and MMAs are drained, and TMEM is freed.
+// TMA (raw weights, the dx rows) go back through release_stage, which fences
+// the reads against the async-proxy refill.  Every wait is bounded: a wait
+// that runs past its deadline raises the CTA's abort flag and QMM_ETIMEOUT in
+// the status word, all roles leave their loops, in-flight copies and MMAs
+// are drained, and TMEM is freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -52,65 +61,85 @@ constexpr int kQ4 = 0, kQ6 = 1;
 
 template <int QT, int BN>
 struct Cfg {
-  static constexpr int BM = 128;
-  // unpack warps.  A 14-warp layout with four caps a thread at 128 registers
-  // and was measured no faster for Q6_K (it also exposed, before the stages
-  // were handed back through release_stage, the cross-proxy refill race that
-  // release_stage closes).
-  static constexpr int NU = 2;
-  static constexpr int UROWS = BM / (32 * NU);  // rows each unpack thread converts per stage
-  static constexpr int EPI0 = 2 + NU;           // first of the 8 epilogue warps
-  static constexpr int THREADS = 32 * (EPI0 + 8);
-  static constexpr int KS = 64;  // k per operand stage
-  static constexpr int RS = 2, AS = 3, BS = 4;
-  // raw bytes per row and super-block in shared memory (Q6_K: a window
-  // around the 2-byte-aligned 210-byte block; 240 rather than 224 bytes, so
-  // that a warp's 32-bit loads of 32 rows hit 8 bank offsets instead of 4)
+  static constexpr int BM = 128;                // weight rows per CTA = TMEM lanes
+  static constexpr int KS = 64;                 // k per operand stage
+  // first unpack warp; epilogue warps per TMEM lane quarter, all epilogue
+  // warps, the first of them
+  static constexpr int U0 = 4, EPQ = 2, NE = 4 * EPQ, E0 = 8;
+  static constexpr int THREADS = 32 * (E0 + NE);
+  static constexpr int CPW = BN / EPQ;  // token columns per epilogue warp
+  static_assert(CPW % 32 == 0, "whole 32-column TMEM loads");
+  // register budgets per warpgroup: producers / MMA (warps 0-3), unpack
+  // (4-7), epilogue (8-).  The block is launched with 65536 / THREADS per
+  // thread, rounded down to a multiple of 8 (128 for 512 threads, 80 for
+  // 768); the budgets add up to no more than that.
+  static constexpr uint32_t REG_LAUNCH = (65536 / THREADS) & ~7u;
+  static constexpr uint32_t REG_CTL = THREADS == 512 ? 56 : 40, REG_UNPACK = THREADS == 512 ? 96 : 80;
+  static constexpr uint32_t REG_EPI = ((REG_LAUNCH * THREADS - 128 * (REG_CTL + REG_UNPACK)) / (32 * NE)) & ~7u;
+  static_assert(128 * (REG_CTL + REG_UNPACK) + 32 * NE * REG_EPI <= REG_LAUNCH * THREADS, "register split");
+  static_assert(REG_EPI >= REG_LAUNCH, "the epilogue gains registers");
+  // ring depths: raw weight super-blocks, activation stages, dx stages,
+  // operand stages in TMEM.  The activation ring is as deep as shared memory
+  // allows: its stages are released by the MMAs alone, so all of them are
+  // prefetch depth against the TMA latency.
+  static constexpr int RS = (QT == kQ6 && BN == 64) ? 4 : 3;
+  static constexpr int BS = BN == 128 ? 6 : 8;
+  static constexpr int DS = 8, AS = 4;
+  // raw bytes per row and super-block in shared memory (Q6_K: a window around
+  // the 2-byte-aligned 210-byte block; 240 rather than 224 bytes, so that a
+  // warp's 32-bit loads of 32 rows hit 8 bank offsets instead of 4)
   static constexpr int RAW_ROW = QT == kQ4 ? 144 : 240;
-  static constexpr int GPS = QT == kQ4 ? 2 : 4;  // scale groups per stage
-  static constexpr int MPG = QT == kQ4 ? 2 : 1;  // K=16 MMAs per group
   static constexpr int RAW_BYTES = BM * RAW_ROW;
-  static constexpr int A_BYTES = BM * KS * 2;
+  static constexpr bool MINT = QT == kQ4;                // Q4_K min term
+  static constexpr int MINB_BYTES = MINT ? BN * 64 : 0;  // 4 chunks x BN tokens x 8 bf16
+  static constexpr int AMIN_BYTES = MINT ? BM * 64 : 0;  // 4 chunks x BM rows x 8 bf16
   static constexpr int B_BYTES = BN * KS * 2;
-  static constexpr int SC_BYTES = 2 * BN * 4;  // dx of the stage's two 32-k groups
-  // Q4_K min term: per super-block the MMA operands m[row][8p + j] (A) and
-  // s_p[token][8p + j] (B, the three bf16 parts of s), k = 32: 4 chunks of 8
-  static constexpr bool MINMMA = QT == kQ4;
-  static constexpr int AMIN_BYTES = MINMMA ? BM * 64 : 0;
-  static constexpr int BMIN_BYTES = MINMMA ? BN * 64 : 0;
-  // TMEM (all 512 columns): NBUF group accumulators of BN columns, then the
-  // min-term accumulator
-  static constexpr int TMEM_COLS = 512;
-  static constexpr int NBUF = TMEM_COLS / BN - (MINMMA ? 1 : 0);
-  static_assert(NBUF <= 8, "accumulator barriers");
+  static constexpr int SC_BYTES = 2 * BN * 4;  // dx of a stage's two 32-value blocks
+  // TMEM: NBUF accumulators of BN columns, then AS operand stages of ACOLS
+  // columns (Q4_K: 32, the codes of 64 k; Q6_K: 64, the hi and lo operands of
+  // two 32-value blocks).  A barrier hop costs ~150 cycles and an MMA's
+  // completion is seen ~250 cycles after its work, so both rings need depth:
+  // four operand stages, and accumulators for 256-512 cycles of tensor work
+  // (a Q6_K block, with its hi and lo operands, is twice a Q4_K block's).
+  static constexpr int ACOLS = QT == kQ4 ? 32 : 64;
+  static constexpr int NBUF = (512 - AS * ACOLS) / BN;
+  static constexpr int A_COL0 = NBUF * BN;
+  static_assert(NBUF >= 2 && NBUF <= 8, "accumulator ring");
+  static_assert(A_COL0 % 16 == 0 && ACOLS % 16 == 0, "TMEM column alignment");
   static constexpr int RAW_OFF = 0;
-  static constexpr int A_OFF = RAW_OFF + RS * RAW_BYTES;
-  static constexpr int B_OFF = A_OFF + AS * A_BYTES;
-  static constexpr int SC_OFF = B_OFF + BS * B_BYTES;
-  static constexpr int AMIN_OFF = SC_OFF + BS * SC_BYTES;
-  static constexpr int BMIN_OFF = AMIN_OFF + RS * AMIN_BYTES;
-  static constexpr int BAR_OFF = BMIN_OFF + RS * BMIN_BYTES;
-  // barriers: raw full/empty, a full/empty, b full/empty, acc full/empty, done, min full/empty
-  static constexpr int NBARS = 2 * RS + 2 * AS + 2 * BS + 16 + 1 + 2;
+  static constexpr int B_OFF = RAW_OFF + RS * RAW_BYTES;
+  static constexpr int MINB_OFF = B_OFF + BS * B_BYTES;
+  // Q4_K: the min term's weight operand m[r][j] (bf16, canonical K-major),
+  // one per raw stage: written by the unpack warps, read by the min MMA
+  static constexpr int AMIN_OFF = MINB_OFF + RS * MINB_BYTES;
+  static constexpr int SC_OFF = AMIN_OFF + RS * AMIN_BYTES;
+  static constexpr int BAR_OFF = SC_OFF + DS * SC_BYTES;
+  // barriers: raw full/empty, b full/empty, dx full/empty, a full/empty,
+  // acc full/empty, done
+  static constexpr int NBARS = 2 * RS + 2 * BS + 2 * DS + 2 * AS + 2 * NBUF + 1;
+  static_assert(BAR_OFF + NBARS * 8 + 16 + 1024 <= 227 * 1024, "shared memory");
   static constexpr int SMEM = BAR_OFF + NBARS * 8 + 16 + 1024;  // + slack for 1 KB alignment
-  static_assert(RAW_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
-  static_assert(SC_BYTES % 16 == 0, "align");
+  static_assert(RAW_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128-byte swizzle needs 1 KB aligned stages");
+  static_assert(SC_BYTES % 16 == 0 && MINB_BYTES % 16 == 0, "bulk copy alignment");
 };
 
+template <int QT, int BN>
 struct Bars {
+  using C = Cfg<QT, BN>;
   uint32_t base;
-  int RS, AS, BS;
   __device__ uint32_t raw_full(int i) const { return base + 8 * i; }
-  __device__ uint32_t raw_empty(int i) const { return base + 8 * (RS + i); }
-  __device__ uint32_t a_full(int i) const { return base + 8 * (2 * RS + i); }
-  __device__ uint32_t a_empty(int i) const { return base + 8 * (2 * RS + AS + i); }
-  __device__ uint32_t b_full(int i) const { return base + 8 * (2 * RS + 2 * AS + i); }
-  __device__ uint32_t b_empty(int i) const { return base + 8 * (2 * RS + 2 * AS + BS + i); }
-  __device__ uint32_t acc_full(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + i); }
-  __device__ uint32_t acc_empty(int i) const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 8 + i); }
-  __device__ uint32_t done() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 16); }
-  __device__ uint32_t min_full() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 17); }
-  __device__ uint32_t min_empty() const { return base + 8 * (2 * RS + 2 * AS + 2 * BS + 18); }
+  __device__ uint32_t raw_empty(int i) const { return base + 8 * (C::RS + i); }
+  __device__ uint32_t b_full(int i) const { return base + 8 * (2 * C::RS + i); }
+  __device__ uint32_t b_empty(int i) const { return base + 8 * (2 * C::RS + C::BS + i); }
+  static constexpr int X0 = 2 * C::RS + 2 * C::BS;  // after the raw and activation rings
+  __device__ uint32_t dx_full(int i) const { return base + 8 * (X0 + i); }
+  __device__ uint32_t dx_empty(int i) const { return base + 8 * (X0 + C::DS + i); }
+  static constexpr int A0 = X0 + 2 * C::DS;
+  __device__ uint32_t a_full(int i) const { return base + 8 * (A0 + i); }
+  __device__ uint32_t a_empty(int i) const { return base + 8 * (A0 + C::AS + i); }
+  __device__ uint32_t acc_full(int i) const { return base + 8 * (A0 + 2 * C::AS + i); }
+  __device__ uint32_t acc_empty(int i) const { return base + 8 * (A0 + 2 * C::AS + C::NBUF + i); }
+  __device__ uint32_t done() const { return base + 8 * (A0 + 2 * C::AS + 2 * C::NBUF); }
 };
 
 // Wait used while draining: ignores the abort flag, gives up at `deadline`.
@@ -121,111 +150,89 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-// Warp-uniform bounded wait: every lane polls, the warp agrees on the outcome.
+// Bounded wait of one thread.  (Waits that park the thread with a suspend
+// hint were measured 3-8 % slower here than polling try_wait.)
+__device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, const Guard& g) {
+  return wait_bar(bar, parity, g);
+}
+
+// Warp-uniform bounded wait: every lane waits, the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Guard& g) {
-  const bool ok = wait_bar(bar, parity, g);
+  const bool ok = gwait(bar, parity, g);
   return __all_sync(0xffffffffu, ok);
 }
 
-// f16x2 of (1024 + a, 1024 + b) for two 4..6-bit codes held in bits 0-5 and 16-21.
+// f16x2 of (1024 + a, 1024 + b) for two codes held in bits 0-5 and 16-21.
 __device__ __forceinline__ uint32_t magic_pair(uint32_t two_codes, uint32_t mask) {
   return and_or(two_codes, mask, 0x64006400u);
 }
 
+__device__ __forceinline__ uint32_t f16x2_of(float v) {
+  const __half2 h = __float2half2_rn(v);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // ---------------------------------------------------------------- unpack --
-// Q4_K: pair p of one row (qs bytes 32p..32p+31) -> 64 f16 operand values in
-// k order: the low nibbles are k 0..31 (sub-block 2p), the high ones k 32..63
-// (sub-block 2p+1).  Each value is sc*nibble (FOLD) or the nibble itself.
-// Output: row-major 8-k chunks at dst + kc*2048 (kc = k/8), 16 bytes each.
-// The 12 words of pair p of one row: the 16-byte header, then qs bytes
-// 32p..32p+31.
-struct Q4Raw {
-  uint4 hdr, q0, q1;
-};
-__device__ __forceinline__ Q4Raw load_q4k_pair(const uint8_t* raw_row, int p) {
-  return {*reinterpret_cast<const uint4*>(raw_row), *reinterpret_cast<const uint4*>(raw_row + 16 + 32 * p),
-          *reinterpret_cast<const uint4*>(raw_row + 16 + 32 * p + 16)};
-}
-
-template <bool FOLD>
-__device__ __forceinline__ void unpack_q4k_pair(const Q4Raw& rw, int p, uint8_t* dst) {
-  const uint4 hdr = rw.hdr, q0 = rw.q0, q1 = rw.q1;
+// Q4_K: stage p of one row (qs bytes 32p..32p+31, i.e. sub-blocks 2p and
+// 2p+1) -> 32 TMEM columns of f16 pairs in k order: column c holds k = 2c and
+// 2c+1; the low nibbles are k 0..31, the high ones k 32..63.  Each value is
+// sc * nibble (an exact f16 integer <= 945), the 1024-magic conversion with
+// the scale folded into the FMA: (1024 + n) * sc - 1024 * sc.
+__device__ __forceinline__ void unpack_q4k_stage(uint4 q0, uint4 q1, uint32_t sc2, bool d_zero,
+                                                 uint32_t (&a)[32]) {
   const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-  uint32_t mul_lo, off_lo, mul_hi, off_hi;
-  if (FOLD) {
-    int sc_lo, m_lo, sc_hi, m_hi;
-    q4k_scale_min_words(hdr.y, hdr.z, hdr.w, 2 * p, sc_lo, m_lo);
-    q4k_scale_min_words(hdr.y, hdr.z, hdr.w, 2 * p + 1, sc_hi, m_hi);
-    if ((hdr.x & 0x7FFFu) == 0) sc_lo = sc_hi = 0;  // d == 0: the main term vanishes
-    const __half2 a = __float2half2_rn((float)sc_lo), b = __float2half2_rn((float)sc_hi);
-    const __half2 na = __float2half2_rn(-1024.0f * (float)sc_lo), nb = __float2half2_rn(-1024.0f * (float)sc_hi);
-    mul_lo = *reinterpret_cast<const uint32_t*>(&a);
-    mul_hi = *reinterpret_cast<const uint32_t*>(&b);
-    off_lo = *reinterpret_cast<const uint32_t*>(&na);
-    off_hi = *reinterpret_cast<const uint32_t*>(&nb);
-  } else {
-    mul_lo = mul_hi = 0x3C003C00u;  // 1.0
-    off_lo = off_hi = 0xE400E400u;  // -1024.0
-  }
+  const float sl = d_zero ? 0.0f : (float)(sc2 & 0xFFu), sh = d_zero ? 0.0f : (float)(sc2 >> 8);
+  const uint32_t mul_lo = f16x2_of(sl), off_lo = f16x2_of(-1024.0f * sl);
+  const uint32_t mul_hi = f16x2_of(sh), off_hi = f16x2_of(-1024.0f * sh);
 #pragma unroll
-  for (int kc = 0; kc < 4; ++kc) {
-    uint32_t lo[4], hi[4];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const uint32_t wd = w[2 * kc + e];
-      const uint32_t t01 = prmt(wd, 0u, 0x4140u), t23 = prmt(wd, 0u, 0x4342u);
-      lo[2 * e] = hfma2_bits(magic_pair(t01, 0x000F000Fu), mul_lo, off_lo);
-      lo[2 * e + 1] = hfma2_bits(magic_pair(t23, 0x000F000Fu), mul_lo, off_lo);
-      hi[2 * e] = hfma2_bits(magic_pair(t01 >> 4, 0x000F000Fu), mul_hi, off_hi);
-      hi[2 * e + 1] = hfma2_bits(magic_pair(t23 >> 4, 0x000F000Fu), mul_hi, off_hi);
-    }
-    *reinterpret_cast<uint4*>(dst + kc * 2048) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    *reinterpret_cast<uint4*>(dst + (kc + 4) * 2048) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t t01 = prmt(w[i], 0u, 0x4140u), t23 = prmt(w[i], 0u, 0x4342u);
+    a[2 * i] = hfma2_bits(magic_pair(t01, 0x000F000Fu), mul_lo, off_lo);
+    a[2 * i + 1] = hfma2_bits(magic_pair(t23, 0x000F000Fu), mul_lo, off_lo);
+    a[16 + 2 * i] = hfma2_bits(magic_pair(t01 >> 4, 0x000F000Fu), mul_hi, off_hi);
+    a[16 + 2 * i + 1] = hfma2_bits(magic_pair(t23 >> 4, 0x000F000Fu), mul_hi, off_hi);
   }
 }
 
-// Q6_K: stage s (elements 64s..64s+63 of the super-block) of one row -> 64
-// f16 values q - 32.  Element 128n + 32*quad + l takes its low 4 bits from
+// Q6_K: one 32-value block of stage s of one row -> 32 TMEM columns: the hi
+// and lo operands of its two 16-value groups, [hi g0 | lo g0 | hi g1 | lo g1],
+// 8 columns (16 k) each.  Stage s holds elements 64s..64s+63 of the
+// super-block: half n = s/2, quads 2(s%2) and 2(s%2)+1 (block `blk` = quad
+// 2(s%2)+blk).  Element 128n + 32*quad + l takes its low 4 bits from
 // ql[64n + l] (quads 0, 2) or ql[64n + 32 + l] (quads 1, 3) -- the low nibble
 // for quads 0-1, the high one for quads 2-3 -- and its top 2 bits from bits
-// 2*quad..2*quad+1 of qh[32n + l].  Stage s covers half n = s/2, quads
-// 2(s%2) and 2(s%2)+1.
-struct Q6Raw {
-  uint32_t L[16], H[8];  // ql bytes 64n..64n+63, qh bytes 32n..32n+31 of half n = s/2
-};
-__device__ __forceinline__ void load_q6k_stage(const uint8_t* row_window, int blk_off, int s, Q6Raw& rw) {
-  const int n = s >> 1;
-  load_words_even<16>(row_window, blk_off + 64 * n, rw.L);
-  load_words_even<8>(row_window, blk_off + 128 + 32 * n, rw.H);
+// 2*quad..2*quad+1 of qh[32n + l].  L: the 8 ql words of this quad's l range,
+// H: the 8 qh words of the half; mh / ml: f16x2 multipliers of the two groups.
+__device__ __forceinline__ void unpack_q6k_block(const uint32_t (&L)[8], const uint32_t (&H)[8], int s, int blk,
+                                                 const uint32_t (&mh)[2], const uint32_t (&ml)[2],
+                                                 uint32_t (&a)[32]) {
+  const uint32_t upper = (uint32_t)(s & 1);
+  const uint32_t quad = 2u * upper + (uint32_t)blk;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int g = w >> 2;  // group of values l = 4w..4w+3
+    const uint32_t codes = ((L[w] >> (4u * upper)) & 0x0F0F0F0Fu) | (((H[w] >> (2u * quad)) << 4) & 0x30303030u);
+    const uint32_t t01 = prmt(codes, 0u, 0x4140u), t23 = prmt(codes, 0u, 0x4342u);
+    // (q - 32) as f16: (1024 + q) - 1056
+    const uint32_t v01 = hfma2_bits(magic_pair(t01, 0x003F003Fu), 0x3C003C00u, 0xE420E420u);
+    const uint32_t v23 = hfma2_bits(magic_pair(t23, 0x003F003Fu), 0x3C003C00u, 0xE420E420u);
+    const int c = 16 * g + 2 * (w & 3);
+    a[c] = hmul2_bits(v01, mh[g]);
+    a[c + 1] = hmul2_bits(v23, mh[g]);
+    a[c + 8] = hmul2_bits(v01, ml[g]);
+    a[c + 9] = hmul2_bits(v23, ml[g]);
+  }
 }
 
-__device__ __forceinline__ void unpack_q6k_stage(const Q6Raw& rw, int s, uint8_t* dst) {
-  const uint32_t* L = rw.L;
-  const uint32_t* H = rw.H;
-  const bool upper = s & 1;
-  const uint32_t mul = 0x3C003C00u, off = 0xE420E420u;  // 1.0, -1056.0 (= -1024 - 32)
-#pragma unroll
-  for (int kc = 0; kc < 8; ++kc) {
-    // kc 0..3: first quad of the stage, l = 8kc..; kc 4..7: second quad, l = 8(kc-4)..
-    const int quad1 = kc >> 2;
-    const int i0 = 2 * (kc & 3);  // word index of l
-    uint32_t v[4];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const uint32_t lw = L[i0 + e + 8 * quad1];
-      const uint32_t hw = H[i0 + e];
-      uint32_t codes;
-      if (!upper) {
-        codes = (lw & 0x0F0F0F0Fu) | ((quad1 ? (hw << 2) : (hw << 4)) & 0x30303030u);
-      } else {
-        codes = ((lw >> 4) & 0x0F0F0F0Fu) | ((quad1 ? (hw >> 2) : hw) & 0x30303030u);
-      }
-      const uint32_t t01 = prmt(codes, 0u, 0x4140u), t23 = prmt(codes, 0u, 0x4342u);
-      v[2 * e] = hfma2_bits(magic_pair(t01, 0x003F003Fu), mul, off);
-      v[2 * e + 1] = hfma2_bits(magic_pair(t23, 0x003F003Fu), mul, off);
-    }
-    *reinterpret_cast<uint4*>(dst + kc * 2048) = make_uint4(v[0], v[1], v[2], v[3]);
-  }
+// The exact split of a signed int8 group scale into the two f16 operand
+// multipliers: hi = sgn * 16 * (|sc| >> 4), lo = sgn * (|sc| & 15), so that
+// hi + lo = sc and every product with q - 32 in [-32, 31] is an exact f16
+// integer.  Both are zero when the super-block's d is zero.
+__device__ __forceinline__ void q6k_split(int sc, bool d_zero, uint32_t& mh, uint32_t& ml) {
+  const int a = sc < 0 ? -sc : sc;
+  const float sg = sc < 0 ? -1.0f : 1.0f;
+  mh = f16x2_of(d_zero ? 0.0f : sg * (float)(16 * (a >> 4)));
+  ml = f16x2_of(d_zero ? 0.0f : sg * (float)(a & 15));
 }
 
 // --------------------------------------------------------------- kernel --
@@ -241,7 +248,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
   const uint32_t pad = (1024u - (s0 & 1023u)) & 1023u;
   uint8_t* smem = smem_dyn + pad;
   const uint32_t sb = s0 + pad;
-  const Bars bars{sb + C::BAR_OFF, C::RS, C::AS, C::BS};
+  const Bars<QT, BN> bars{sb + C::BAR_OFF};
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + C::NBARS * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + C::NBARS * 8 + 4);
 
@@ -251,29 +258,32 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
   // ring indices below are relative to the slice, addresses absolute
   const int nsb_all = K >> 8, per = (nsb_all + (int)gridDim.z - 1) / (int)gridDim.z;
   const int b_off = (int)blockIdx.z * per;
-  const int nsb = min(per, nsb_all - b_off), NS = 4 * nsb;
+  const int nsb = min(per, nsb_all - b_off);
   const Guard g{abort_flag, status, global_ns() + (uint64_t)limit_ms * 1000000ull};
+  constexpr bool MIN = C::MINT && !DOTS;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::RS; ++i) {
       mbar_init(bars.raw_full(i), 1);
-      mbar_init(bars.raw_empty(i), C::NU + (C::MINMMA && !DOTS ? 1 : 0));  // unpack warps (+ the min-term MMAs)
-    }
-    for (int i = 0; i < C::AS; ++i) {
-      mbar_init(bars.a_full(i), C::NU);
-      mbar_init(bars.a_empty(i), 1);
+      mbar_init(bars.raw_empty(i), 4 + (MIN ? 1 : 0));  // unpack warps (+ the min-term MMAs)
     }
     for (int i = 0; i < C::BS; ++i) {
       mbar_init(bars.b_full(i), 1);
-      mbar_init(bars.b_empty(i), 1 + 8);
+      mbar_init(bars.b_empty(i), 1);  // the MMAs that read the stage have completed
+    }
+    for (int i = 0; i < C::DS; ++i) {
+      mbar_init(bars.dx_full(i), 1);
+      mbar_init(bars.dx_empty(i), C::NE);  // the epilogue warps read the stage's dx rows
+    }
+    for (int i = 0; i < C::AS; ++i) {
+      mbar_init(bars.a_full(i), 4);
+      mbar_init(bars.a_empty(i), 1);
     }
     for (int i = 0; i < C::NBUF; ++i) {
       mbar_init(bars.acc_full(i), 1);
-      mbar_init(bars.acc_empty(i), 8);
+      mbar_init(bars.acc_empty(i), C::NE);
     }
     mbar_init(bars.done(), 1);
-    mbar_init(bars.min_full(), 1);
-    mbar_init(bars.min_empty(), 8);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -283,7 +293,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                 "r"(C::TMEM_COLS)
+                 "r"(512)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -292,46 +302,46 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const uint32_t raw_s = sb + C::RAW_OFF, a_s = sb + C::A_OFF, b_s = sb + C::B_OFF, sc_s = sb + C::SC_OFF;
-  const uint32_t amin_s = sb + C::AMIN_OFF, bmin_s = sb + C::BMIN_OFF;
+  const uint32_t raw_s = sb + C::RAW_OFF, b_s = sb + C::B_OFF, sc_s = sb + C::SC_OFF, minb_s = sb + C::MINB_OFF;
+  const uint32_t amin_s = sb + C::AMIN_OFF;
   // the bf16 parts of s: [K/256][4][ntp][8] after the dx plane [K/32][ntp]
   const uint8_t* smin = reinterpret_cast<const uint8_t*>(scl + (size_t)(K >> 5) * ntp);
-  constexpr bool MIN = C::MINMMA && !DOTS;
 
+  // Each warpgroup sets its register budget at the top of its own branch, so
+  // that the budget covers all of the role's code.
+  if (warp < C::U0) {
+    regs_release<C::REG_CTL>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t nbytes_b = (uint64_t)C::B_BYTES + C::SC_BYTES;
+      // everything loaded below may be written by the preceding kernel
+      griddep_wait();
       int raw_issued = 0, b_issued = 0;
       bool ok = true;
       for (int b = 0; b < nsb && ok; ++b) {
         const int rs = b % C::RS;
-        if (!wait_bar(bars.raw_empty(rs), ((b / C::RS) & 1) ^ 1, g)) break;
+        if (!gwait(bars.raw_empty(rs), ((b / C::RS) & 1) ^ 1, g)) break;
         if (!(skip_first_weight_load && b == 0)) {
-          mbar_arrive_expect_tx(bars.raw_full(rs), C::RAW_BYTES + (MIN ? 4 * BN * 16 : 0));
+          mbar_arrive_expect_tx(bars.raw_full(rs), C::RAW_BYTES + (MIN ? C::MINB_BYTES : 0));
           const int x = QT == kQ4 ? (b + b_off) * kQ4KBytes : ((b + b_off) * kQ6KBytes) & ~15;
           tma_load_2d(raw_s + rs * C::RAW_BYTES, &tmW, x, row0, bars.raw_full(rs));
           if (MIN) {
 #pragma unroll
             for (int kc = 0; kc < 4; ++kc)
-              bulk_load(bmin_s + rs * C::BMIN_BYTES + kc * BN * 16,
+              bulk_load(minb_s + rs * C::MINB_BYTES + kc * BN * 16,
                         smin + (((size_t)(b + b_off) * 4 + kc) * ntp + tok0) * 16, BN * 16, bars.raw_full(rs));
           }
         }
         ++raw_issued;
         for (int s = 0; s < 4; ++s) {
           const int gs = 4 * b + s, bs = gs % C::BS;
-          if (!wait_bar(bars.b_empty(bs), ((gs / C::BS) & 1) ^ 1, g)) {
+          if (!gwait(bars.b_empty(bs), ((gs / C::BS) & 1) ^ 1, g)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bars.b_full(bs), (uint32_t)nbytes_b);
+          mbar_arrive_expect_tx(bars.b_full(bs), (uint32_t)C::B_BYTES);
           const int gk = gs + 4 * b_off;  // absolute 64-k stage
           tma_load_2d(b_s + bs * C::B_BYTES, &tmX, C::KS * gk, tok0, bars.b_full(bs));
-#pragma unroll
-          for (int gi = 0; gi < 2; ++gi)
-            bulk_load(sc_s + bs * C::SC_BYTES + gi * BN * 4, scl + ((size_t)(2 * gk + gi) * ntp + tok0),
-                      BN * 4, bars.b_full(bs));
           ++b_issued;
         }
       }
@@ -343,288 +353,364 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
       for (int i = b_issued - C::BS; i < b_issued; ++i)
         if (i >= 0) drain_wait(bars.b_full(i % C::BS), (i / C::BS) & 1, dl);
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------- dx producer
+    // the token-contiguous dx rows of each stage's two 32-value blocks, in
+    // their own ring: the epilogue releases them, the MMAs do not wait on it
+    if (lane == 0) {
+      griddep_wait();
+      int issued = 0;
+      for (int gs = 0; gs < 4 * nsb; ++gs) {
+        const int ds = gs % C::DS;
+        if (!gwait(bars.dx_empty(ds), ((gs / C::DS) & 1) ^ 1, g)) break;
+        mbar_arrive_expect_tx(bars.dx_full(ds), (uint32_t)C::SC_BYTES);
+        const int gk = gs + 4 * b_off;
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi)
+          bulk_load(sc_s + ds * C::SC_BYTES + gi * BN * 4, scl + ((size_t)(2 * gk + gi) * ntp + tok0), BN * 4,
+                    bars.dx_full(ds));
+        ++issued;
+      }
+      const uint64_t dl = global_ns() + 1000000000ull;
+      for (int i = issued - C::DS; i < issued; ++i)
+        if (i >= 0) drain_wait(bars.dx_full(i % C::DS), (i / C::DS) & 1, dl);
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA
+    // One thread issues every MMA of the CTA, so its loop is kept lean: the
+    // stage structure of a super-block is unrolled, ring positions are
+    // counters, and the shared-memory descriptors are advanced by constant
+    // offsets (a single issuing thread would otherwise spend several times
+    // an MMA's duration on index arithmetic between two MMAs).
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(C::BM, BN);
-      int u = 0;
+      constexpr uint32_t idesc = idesc_f16(C::BM, BN);
+      constexpr uint32_t idesc_bf = idesc | (1u << 7) | (1u << 10);  // A and B bf16
+      // descriptor start addresses are in 16-byte units in the low bits
+      const uint64_t bdesc0 = smem_desc(b_s, 16, 1024, 2);
+      const uint64_t mdesc0 = smem_desc(minb_s, BN * 16, 128, 0);
+      const uint64_t adesc0 = smem_desc(amin_s, 2048, 128, 0);
+      uint32_t slot = 0, ph = 0;  // accumulator ring position and the parity of its round
+      int bs = 0, rs = 0;
+      uint32_t bph = 0;
       bool ok = true;
-      for (int gs = 0; gs < NS && ok; ++gs) {
-        const int as = gs % C::AS, bs = gs % C::BS;
-        if (!wait_bar(bars.a_full(as), (gs / C::AS) & 1, g)) break;
-        if (!wait_bar(bars.b_full(bs), (gs / C::BS) & 1, g)) break;
+      // the next accumulator, once the epilogue has read it: its TMEM address
+      auto acquire = [&](uint32_t& d_t) -> bool {
+        if (!gwait(bars.acc_empty(slot), ph ^ 1u, g)) return false;
         tc_fence_after();
-        for (int gi = 0; gi < C::GPS; ++gi, ++u) {
-          const int buf = u % C::NBUF;
-          if (!wait_bar(bars.acc_empty(buf), ((u / C::NBUF) & 1) ^ 1, g)) {
+        d_t = tmem + slot * (uint32_t)BN;
+        return true;
+      };
+      auto advance = [&]() {
+        if (++slot == (uint32_t)C::NBUF) {
+          slot = 0;
+          ph ^= 1u;
+        }
+      };
+      for (int b = 0; b < nsb && ok; ++b) {
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const int as = s;  // stage 4b + s uses operand slot s in round b
+          if (!gwait(bars.a_full(as), (uint32_t)b & 1u, g) || !gwait(bars.b_full(bs), bph, g)) {
             ok = false;
             break;
           }
           tc_fence_after();
-#pragma unroll
-          for (int i = 0; i < C::MPG; ++i) {
-            const int kk = gi * C::MPG + i;  // K=16 chunk within the 64-k stage
-            const uint64_t ad = smem_desc(a_s + as * C::A_BYTES + kk * 4096, 2048, 128, 0);
-            const uint64_t bd = smem_desc(b_s + bs * C::B_BYTES + kk * 32, 16, 1024, 2);
-            tc_mma_f16(tmem + (uint32_t)(buf * BN), ad, bd, idesc, i > 0 ? 1u : 0u);
+          const uint32_t a_t = tmem + (uint32_t)(C::A_COL0 + as * C::ACOLS);
+          const uint64_t bd = bdesc0 + (uint64_t)(bs * (C::B_BYTES >> 4));
+          uint32_t d_t;
+          if (MIN && s == 0) {
+            // super-block b: D_min[r][t] = sum over its 8 sub-blocks j of
+            // m[r][j] * s[t][j], with s split into three bf16 parts (exact
+            // products, f32 sums)
+            if (!acquire(d_t)) {
+              ok = false;
+              break;
+            }
+            const uint64_t md = mdesc0 + (uint64_t)(rs * (C::MINB_BYTES >> 4));
+            const uint64_t ad = adesc0 + (uint64_t)(rs * (C::AMIN_BYTES >> 4));
+            tc_mma_f16(d_t, ad, md, idesc_bf, 0u);
+            tc_mma_f16(d_t, ad + (uint64_t)((2 * 2048) >> 4), md + (uint64_t)((2 * BN * 16) >> 4), idesc_bf, 1u);
+            tc_commit(bars.acc_full(slot));
+            tc_commit(bars.raw_empty(rs));  // the raw stage's min operands were read
+            advance();
           }
-          tc_commit(bars.acc_full(buf));
-        }
-        if (!ok) break;
-        tc_commit(bars.a_empty(as));
-        tc_commit(bars.b_empty(bs));
-        if (MIN && (gs & 3) == 3) {
-          // super-block b: D_min[r][t] = sum over its 8 sub-blocks j of
-          // m[r][j] * s[t][j], with s split into three bf16 parts (exact
-          // products, f32 sums); then the raw stage (and these operands) may go
-          const int b = gs >> 2, rs = b % C::RS;
-          if (!wait_bar(bars.min_empty(), (b & 1) ^ 1, g)) break;
-          tc_fence_after();
-          const uint32_t idesc_bf = idesc_f16(C::BM, BN) | (1u << 7) | (1u << 10);  // A and B bf16
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t ad = smem_desc(amin_s + rs * C::AMIN_BYTES + kk * 4096, 2048, 128, 0);
-            const uint64_t bd = smem_desc(bmin_s + rs * C::BMIN_BYTES + kk * 2 * BN * 16, BN * 16, 128, 0);
-            tc_mma_f16(tmem + (uint32_t)(C::NBUF * BN), ad, bd, idesc_bf, kk > 0 ? 1u : 0u);
+          for (int gi = 0; gi < 2; ++gi) {
+            if (!acquire(d_t)) {
+              ok = false;
+              break;
+            }
+            if constexpr (QT == kQ4) {
+              // sub-block 2p + gi: k 32gi..32gi+31 of the stage, two K=16 MMAs
+#pragma unroll
+              for (int i = 0; i < 2; ++i)
+                tc_mma_f16_tmem_a(d_t, a_t + 16 * gi + 8 * i, bd + (uint64_t)(2 * (2 * gi + i)), idesc,
+                                  i > 0 ? 1u : 0u);
+            } else {
+              // block gi: hi and lo operands of its groups g0 (k 0..15) and g1
+              // (k 16..31), each against the group's activation codes
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                tc_mma_f16_tmem_a(d_t, a_t + 32 * gi + 8 * i, bd + (uint64_t)(2 * (2 * gi + (i >> 1))), idesc,
+                                  i > 0 ? 1u : 0u);
+            }
+            tc_commit(bars.acc_full(slot));
+            advance();
           }
-          tc_commit(bars.min_full());
-          tc_commit(bars.raw_empty(rs));
+          if (!ok) break;
+          tc_commit(bars.a_empty(as));  // the operand stage in TMEM may be rewritten
+          tc_commit(bars.b_empty(bs));  // and the activation stage refilled
+          if (++bs == C::BS) {
+            bs = 0;
+            bph ^= 1u;
+          }
         }
+        if (++rs == C::RS) rs = 0;
       }
       tc_commit(bars.done());
       drain_wait(bars.done(), 0, global_ns() + 1000000000ull);
     }
-  } else if (warp < C::EPI0) {
+  }
+  } else if (warp < C::E0) {
+    if constexpr (C::REG_UNPACK < C::REG_LAUNCH) regs_release<C::REG_UNPACK>();
     // ----------------------------------------------------------- unpack
-    const int ut = threadIdx.x - 64;  // rows ut + 32 * NU * rr, rr < UROWS
+    const int q = warp & 3;       // TMEM lane quarter
+    const int r = 32 * q + lane;  // the thread's weight row within the tile
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    int rs = 0;
+    uint32_t rph = 0;  // parity of the raw ring's round
     bool ok = true;
     for (int b = 0; b < nsb && ok; ++b) {
-      const int rs = b % C::RS;
-      if (!warp_wait(bars.raw_full(rs), (b / C::RS) & 1, g)) break;
-      const uint8_t* raw = smem + C::RAW_OFF + rs * C::RAW_BYTES;
-      for (int s = 0; s < 4; ++s) {
-        const int gs = 4 * b + s, as = gs % C::AS;
-        if (!warp_wait(bars.a_empty(as), ((gs / C::AS) & 1) ^ 1, g)) {
-          ok = false;
-          break;
-        }
-        uint8_t* a = smem + C::A_OFF + as * C::A_BYTES;
-        if (MIN && s == 0) {
-          // m[r][j] of the 8 sub-blocks as bf16 (exact small integers), the
-          // same 16 bytes for parts 0, 1, 2, zeros for the fourth chunk
-#pragma unroll
-          for (int rr = 0; rr < C::UROWS; ++rr) {
-            const int r = ut + 32 * C::NU * rr;
-            const uint4 hdr = *reinterpret_cast<const uint4*>(raw + r * C::RAW_ROW);
-            uint32_t mw[4];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              uint32_t sc2, m2;
-              q4k_pair_codes(hdr.y, hdr.z, hdr.w, p, sc2, m2);
-              mw[p] = (__float_as_uint((float)(m2 & 0xFFu)) >> 16) | (__float_as_uint((float)(m2 >> 8)) & 0xFFFF0000u);
-            }
-            uint8_t* am = smem + C::AMIN_OFF + rs * C::AMIN_BYTES + r * 16;
-            const uint4 v = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-            *reinterpret_cast<uint4*>(am) = v;
-            *reinterpret_cast<uint4*>(am + 2048) = v;
-            *reinterpret_cast<uint4*>(am + 4096) = v;
-            *reinterpret_cast<uint4*>(am + 6144) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        // all rows' raw words first, then the conversions and stores: the
-        // compiler cannot move a later row's loads above an earlier row's
-        // stores (both are shared memory), so this overlaps their latency
-        if constexpr (QT == kQ4) {
-          Q4Raw rw[C::UROWS];
-#pragma unroll
-          for (int rr = 0; rr < C::UROWS; ++rr) rw[rr] = load_q4k_pair(raw + (ut + 32 * C::NU * rr) * C::RAW_ROW, s);
-#pragma unroll
-          for (int rr = 0; rr < C::UROWS; ++rr) unpack_q4k_pair<!DOTS>(rw[rr], s, a + (ut + 32 * C::NU * rr) * 16);
-        } else {
-          const int blk_off = ((b + b_off) * kQ6KBytes) & 15;
-          Q6Raw rw[C::UROWS];
-#pragma unroll
-          for (int rr = 0; rr < C::UROWS; ++rr)
-            load_q6k_stage(raw + (ut + 32 * C::NU * rr) * C::RAW_ROW, blk_off, s, rw[rr]);
-#pragma unroll
-          for (int rr = 0; rr < C::UROWS; ++rr) unpack_q6k_stage(rw[rr], s, a + (ut + 32 * C::NU * rr) * 16);
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.a_full(as));
-      }
-      if (!ok) break;
-      release_stage(bars.raw_empty(rs));
-    }
-  } else {
-    // --------------------------------------------------------- epilogue
-    const int q = warp & 3;               // TMEM lane quarter this warp may read
-    const int hc = (warp - C::EPI0) >> 2;  // column half
-    const int r = 32 * q + lane;          // tile row
-    const int row_g = row0 + r;
-    const bool row_ok = row_g < od;
-    const int row_c = row_ok ? row_g : od - 1;
-    constexpr int HALF = BN / 2;
-    constexpr int CH = HALF / 32;
-    const size_t row_bytes = (size_t)nsb_all * (QT == kQ4 ? kQ4KBytes : kQ6KBytes);
-    const uint8_t* wrow = W + (size_t)row_c * row_bytes;
-    // Q4_K: one f32 per token of the warp's columns (one FMA per output and
-    // group, measured faster than packed pairs); Q6_K: packed pairs of tokens
-    // (2i, 2i + 1), so the group's scale multiply and the FMA take one
-    // instruction per two outputs each
-    constexpr bool PK = QT != kQ4;
-    float acc[PK ? 1 : HALF];
-    f2 acc2[PK ? HALF / 2 : 1];
-#pragma unroll
-    for (int i = 0; i < (PK ? 1 : HALF); ++i) acc[i] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < (PK ? HALF / 2 : 1); ++i) acc2[i] = 0ull;
-    float sigma = 1.0f;  // acc holds (partial sum) / sigma
-    int u = 0;
-    bool ok = true;
-    // the next super-block's scale words are fetched one super-block ahead,
-    // so their global-load latency is off the epilogue's critical path
-    uint4 hdr_next = make_uint4(0, 0, 0, 0);  // Q4_K: d, dmin and the 12 packed scale bytes
-    uint32_t sw_next[9] = {};                 // Q6_K: the 16 int8 scales as 8 half-words, then d
-    auto fetch_scales = [&](int bb) {
-      if (DOTS || bb >= nsb) return;
-      if (QT == kQ4) {
-        hdr_next = __ldg(reinterpret_cast<const uint4*>(wrow + (size_t)(bb + b_off) * kQ4KBytes));
+      if (!warp_wait(bars.raw_full(rs), rph, g)) break;
+      const uint8_t* row = smem + C::RAW_OFF + rs * C::RAW_BYTES + r * C::RAW_ROW;
+      // per super-block: Q4_K header (d, dmin, scales); Q6_K scales and d
+      uint4 hdr = make_uint4(0, 0, 0, 0);
+      uint32_t d6 = 0;
+      int blk_off = 0;
+      if constexpr (QT == kQ4) {
+        hdr = *reinterpret_cast<const uint4*>(row);
       } else {
-        const uint16_t* hs = reinterpret_cast<const uint16_t*>(wrow + (size_t)(bb + b_off) * kQ6KBytes + 192);
-#pragma unroll
-        for (int i = 0; i < 9; ++i) sw_next[i] = __ldg(hs + i);
+        blk_off = ((b + b_off) * kQ6KBytes) & 15;
+        d6 = *reinterpret_cast<const uint16_t*>(row + blk_off + 208);
       }
-    };
-    fetch_scales(0);
-    for (int b = 0; b < nsb && ok; ++b) {
-      float gcoef[QT == kQ4 ? 1 : 16];  // Q4_K: -dmin / sigma; Q6_K: the groups' scales
-      if (!DOTS) {
-        const uint4 hdr = hdr_next;
-        uint32_t sw[9];
-#pragma unroll
-        for (int i = 0; i < 9; ++i) sw[i] = sw_next[i];
-        fetch_scales(b + 1);
-        // the rescaling factors only feed the fp32 sums, so a reciprocal
-        // within an ulp or two (instead of an IEEE division) is enough
-        const float d = half_bits_to_float(QT == kQ4 ? hdr.x : sw[8]);
-        if (d != 0.0f) {
-          const float ratio = sigma * __fdividef(1.0f, d);
-          sigma = d;
-          if (b > 0) {
-            if constexpr (PK) {
-              const f2 r2 = pk2(ratio, ratio);
-#pragma unroll
-              for (int i = 0; i < HALF / 2; ++i) acc2[i] = mul2(acc2[i], r2);
-            } else {
-#pragma unroll
-              for (int i = 0; i < HALF; ++i) acc[i] *= ratio;
-            }
-          }
-        }
-        if (QT == kQ4) {
-          gcoef[0] = -half_bits_to_float(hdr.x >> 16) * __fdividef(1.0f, sigma);  // -dmin / sigma
-        } else {
-#pragma unroll
-          for (int gg = 0; gg < 16; ++gg) {
-            const int sc = (int)(int8_t)((sw[gg >> 1] >> (8 * (gg & 1))) & 0xFF);
-            gcoef[gg] = d != 0.0f ? (float)sc : 0.0f;
-          }
-        }
-      }
-#pragma unroll
+      // a rolled loop: the unpack, epilogue and MMA roles run different code
+      // at the same time, and unrolled copies of these bodies would not fit
+      // the instruction cache together
+#pragma unroll 1
       for (int s = 0; s < 4; ++s) {
-        const int gs = 4 * b + s, bs = gs % C::BS;
-        if (!warp_wait(bars.b_full(bs), (gs / C::BS) & 1, g)) {
-          ok = false;
-          break;
-        }
-        const float* scp = reinterpret_cast<const float*>(smem + C::SC_OFF + bs * C::SC_BYTES);
-#pragma unroll
-        for (int gi = 0; gi < C::GPS; ++gi, ++u) {
-          const int buf = u % C::NBUF;
-          if (!warp_wait(bars.acc_full(buf), (u / C::NBUF) & 1, g)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // one 32-column chunk at a time: load, wait, use (32 live
-          // registers of TMEM data instead of BN/2, so nothing spills)
-          const int sub = QT == kQ4 ? gi : (gi >> 1);  // 32-value sub-block within the stage
-          const float* sg = scp + sub * BN + hc * HALF;  // dx of this group's tokens
-          const float coef = DOTS || QT == kQ4 ? 1.0f : gcoef[4 * s + gi];
-          const f2 coef2 = pk2(coef, coef);
-#pragma unroll
-          for (int c = 0; c < CH; ++c) {
-            uint32_t P[32];
-            __syncwarp();
-            tc_ld_32x32_sync(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + hc * HALF + 32 * c), P);
-            if (DOTS) {
-              const int ng = QT == kQ4 ? (K >> 5) : (K >> 4);
-              const int grp = QT == kQ4 ? 8 * (b + b_off) + 2 * s + gi : 16 * (b + b_off) + 4 * s + gi;
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int t = tok0 + hc * HALF + 32 * c + i;
-                if (row_ok && t < nt)
-                  dots[((size_t)t * od + row_g) * ng + grp] = __float2int_rn(__uint_as_float(P[i]));
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                const float4 v = *reinterpret_cast<const float4*>(sg + 32 * c + i);
-                if constexpr (PK) {  // Q6_K: dx times the group's scale, then the FMA
-                  const f2 dx01 = mul2(pk2(v.x, v.y), coef2), dx23 = mul2(pk2(v.z, v.w), coef2);
-                  f2& a01 = acc2[(32 * c + i) / 2];
-                  f2& a23 = acc2[(32 * c + i) / 2 + 1];
-                  a01 = fma2(dx01, pk2(__uint_as_float(P[i]), __uint_as_float(P[i + 1])), a01);
-                  a23 = fma2(dx23, pk2(__uint_as_float(P[i + 2]), __uint_as_float(P[i + 3])), a23);
-                } else {  // Q4_K: the group's scale is folded into the weight operand
-                  static_assert(QT == kQ4, "the scalar form has no group scale");
-                  const float dx[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                  for (int e = 0; e < 4; ++e)
-                    acc[32 * c + i + e] = fmaf(dx[e], __uint_as_float(P[i + e]), acc[32 * c + i + e]);
-                }
-              }
-            }
-          }
-          // hand the accumulator back only now, after its values were used
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars.acc_empty(buf));
-        }
-        if (!ok) break;
-        release_stage(bars.b_empty(bs));  // the stage's dx rows were read
-      }
-      if (MIN && ok) {
-        // the super-block's min term: acc += (-dmin / sigma) * D_min
-        if (!warp_wait(bars.min_full(), b & 1, g)) {
+        const int as = s;
+        // the operand stage in TMEM is free again
+        if (!warp_wait(bars.a_empty(as), ((uint32_t)b & 1u) ^ 1u, g)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float mc = gcoef[0];
+        const uint32_t a_t = tmem + lane_base + (uint32_t)(C::A_COL0 + as * C::ACOLS);
+        if constexpr (QT == kQ4) {
+          const uint4 q0 = *reinterpret_cast<const uint4*>(row + 16 + 32 * s);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(row + 32 + 32 * s);
+          uint32_t sc2, m2;
+          q4k_pair_codes(hdr.y, hdr.z, hdr.w, s, sc2, m2);
+          uint32_t a[32];
+          unpack_q4k_stage(q0, q1, sc2, (hdr.x & 0x7FFFu) == 0, a);
+          tc_st_32x32_x32(a_t, a);
+          if (MIN && s == 0) {
+            // m[r][j] of the 8 sub-blocks as bf16 (exact small integers): k =
+            // 8*part + j for the three parts of s, zeros for the fourth chunk
+            // (shared memory: the raw stage's min operand)
+            uint32_t mv[16];
 #pragma unroll
-        for (int c = 0; c < CH; ++c) {
-          uint32_t Q[32];
-          __syncwarp();
-          tc_ld_32x32_sync(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::NBUF * BN + hc * HALF + 32 * c), Q);
+            for (int p = 0; p < 4; ++p) {
+              uint32_t sc2p, m2p;
+              q4k_pair_codes(hdr.y, hdr.z, hdr.w, p, sc2p, m2p);
+              const uint32_t pr = (__float_as_uint((float)(m2p & 0xFFu)) >> 16) |
+                                  (__float_as_uint((float)(m2p >> 8)) & 0xFFFF0000u);
+              mv[p] = mv[4 + p] = mv[8 + p] = pr;
+              mv[12 + p] = 0u;
+            }
+            // chunk p of the canonical K-major layout at p * 2048, row r at r * 16
+            uint8_t* am = smem + C::AMIN_OFF + rs * C::AMIN_BYTES + r * 16;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(mc, __uint_as_float(Q[i]), acc[32 * c + i]);
+            for (int p = 0; p < 4; ++p)
+              *reinterpret_cast<uint4*>(am + p * 2048) = make_uint4(mv[4 * p], mv[4 * p + 1], mv[4 * p + 2], mv[4 * p + 3]);
+            fence_proxy_async();  // generic writes, read by the MMA through the async proxy
+          }
+        } else {
+          const int n = s >> 1;
+          uint32_t H[8], sw[1];
+          load_words_even<8>(row, blk_off + 128 + 32 * n, H);
+          load_words_even<1>(row, blk_off + 192 + 4 * s, sw);  // the scales of groups 4s..4s+3
+          const bool dz = (d6 & 0x7FFFu) == 0;
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            uint32_t L[8];
+            load_words_even<8>(row, blk_off + 64 * n + 32 * blk, L);
+            // groups 4s + 2blk and 4s + 2blk + 1: bytes 2blk, 2blk+1 of scale word s
+            uint32_t mh[2], ml[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              q6k_split((int)(int8_t)((sw[0] >> (8 * (2 * blk + h))) & 0xFFu), dz, mh[h], ml[h]);
+            uint32_t a[32];
+            unpack_q6k_block(L, H, s, blk, mh, ml, a);
+            tc_st_32x32_x32(a_t + 32 * blk, a);
+          }
         }
-        // hand the accumulator back only after its values were used
+        tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars.min_empty());
+        if (lane == 0) mbar_arrive(bars.a_full(as));
+      }
+      if (!ok) break;
+      release_stage(bars.raw_empty(rs));  // the super-block's raw words were read
+      if (++rs == C::RS) {
+        rs = 0;
+        rph ^= 1u;
+      }
+    }
+  } else {
+    if constexpr (C::REG_EPI > C::REG_LAUNCH) regs_take<C::REG_EPI>();
+    // --------------------------------------------------------- epilogue
+    const int q = warp & 3;              // TMEM lane quarter this warp may read
+    const int cb = (warp - C::E0) >> 2;  // column block: tokens cb*CPW .. + CPW
+    const int r = 32 * q + lane;         // tile row
+    const int row_g = row0 + r;
+    const bool row_ok = row_g < od;
+    const int row_c = row_ok ? row_g : od - 1;
+    constexpr int CPW = C::CPW, CH = CPW / 32;
+    const size_t row_bytes = (size_t)nsb_all * (QT == kQ4 ? kQ4KBytes : kQ6KBytes);
+    const uint8_t* wrow = W + (size_t)row_c * row_bytes;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    float acc[CPW];
+#pragma unroll
+    for (int i = 0; i < CPW; ++i) acc[i] = 0.0f;
+    float sigma = 1.0f;  // acc holds (partial sum) / sigma
+    uint32_t slot = 0, ph = 0;
+    int bs = 0;
+    uint32_t bph = 0;
+    bool ok = true;
+    // the weights (scale words) and the outputs may be touched by the
+    // preceding kernel
+    griddep_wait();
+    // the next super-block's scale words are fetched one super-block ahead,
+    // so their global-load latency is off the epilogue's critical path
+    uint32_t h_next = 0;  // Q4_K: d | dmin << 16; Q6_K: d
+    auto fetch = [&](int bb) {
+      if (DOTS || bb >= nsb) return;
+      if (QT == kQ4)
+        h_next = __ldg(reinterpret_cast<const uint32_t*>(wrow + (size_t)(bb + b_off) * kQ4KBytes));
+      else
+        h_next = __ldg(reinterpret_cast<const uint16_t*>(wrow + (size_t)(bb + b_off) * kQ6KBytes + 208));
+    };
+    // one accumulator entry: wait, read this warp's CPW columns 32 at a time,
+    // hand the accumulator back right after the last read (the values are in
+    // registers), apply f(chunk, P) to each chunk
+    auto entry = [&](auto&& f) -> bool {
+      if (!warp_wait(bars.acc_full(slot), ph, g)) return false;
+      tc_fence_after();
+      const uint32_t t_acc = tmem + lane_base + slot * (uint32_t)BN + (uint32_t)(cb * CPW);
+      const uint32_t bar_empty = bars.acc_empty(slot);
+      if (++slot == (uint32_t)C::NBUF) {
+        slot = 0;
+        ph ^= 1u;
+      }
+      if constexpr (CH == 2) {
+        // both 32-column chunks with one wait, then the accumulator goes back
+        uint32_t P2[64];
+        __syncwarp();
+        tc_ld_32x32_x2_sync(t_acc, P2);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty);
+        f(0, *reinterpret_cast<const uint32_t(*)[32]>(&P2[0]));
+        f(1, *reinterpret_cast<const uint32_t(*)[32]>(&P2[32]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          uint32_t P[32];
+          __syncwarp();
+          tc_ld_32x32_sync(t_acc + 32 * c, P);
+          if (c == CH - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty);
+          }
+          f(c, P);
+        }
+      }
+      return true;
+    };
+    fetch(0);
+    for (int b = 0; b < nsb && ok; ++b) {
+      float mc = 0.0f;  // Q4_K: -dmin / sigma
+      if (!DOTS) {
+        const uint32_t h = h_next;
+        fetch(b + 1);
+        // the rescaling factors only feed the fp32 sums, so a reciprocal
+        // within an ulp or two (instead of an IEEE division) is enough
+        const float d = half_bits_to_float(h);
+        if (d != 0.0f) {
+          const float ratio = sigma * __fdividef(1.0f, d);
+          sigma = d;
+          if (b > 0) {
+#pragma unroll
+            for (int i = 0; i < CPW; ++i) acc[i] *= ratio;
+          }
+        }
+        if (QT == kQ4) mc = -half_bits_to_float(h >> 16) * __fdividef(1.0f, sigma);
+      }
+#pragma unroll 1
+      for (int s = 0; s < 4 && ok; ++s) {
+        if (!warp_wait(bars.dx_full(bs), bph, g)) {
+          ok = false;
+          break;
+        }
+        if (MIN && s == 0) {
+          ok = entry([&](int c, const uint32_t(&P)[32]) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(mc, __uint_as_float(P[i]), acc[32 * c + i]);
+          });
+          if (!ok) break;
+        }
+        const float* scp = reinterpret_cast<const float*>(smem + C::SC_OFF + bs * C::SC_BYTES);
+#pragma unroll
+        for (int gi = 0; gi < 2 && ok; ++gi) {
+          const float* dxp = scp + gi * BN + cb * CPW;  // dx of this block's tokens
+          const int grp = 8 * (b + b_off) + 2 * s + gi;  // the 32-value block within the row
+          ok = entry([&](int c, const uint32_t(&P)[32]) {
+            if constexpr (DOTS) {
+              const size_t ng = (size_t)(K >> 5), tstride = (size_t)od * ng;
+              const int t0 = tok0 + cb * CPW + 32 * c;
+              int32_t* dp = dots + ((size_t)t0 * od + row_g) * ng + grp;
+              const int nv = row_ok ? min(32, nt - t0) : 0;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nv) dp[i * tstride] = __float2int_rn(__uint_as_float(P[i]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(dxp + 32 * c + i);
+                float* a = acc + 32 * c + i;
+                a[0] = fmaf(v.x, __uint_as_float(P[i]), a[0]);
+                a[1] = fmaf(v.y, __uint_as_float(P[i + 1]), a[1]);
+                a[2] = fmaf(v.z, __uint_as_float(P[i + 2]), a[2]);
+                a[3] = fmaf(v.w, __uint_as_float(P[i + 3]), a[3]);
+              }
+            }
+          });
+        }
+        if (!ok) break;
+        release_stage(bars.dx_empty(bs));  // the stage's dx rows were read
+        if (++bs == C::DS) {
+          bs = 0;
+          bph ^= 1u;
+        }
       }
     }
     if (!DOTS && ok && row_ok) {
 #pragma unroll
-      for (int i = 0; i < HALF; i += 2) {
-        const float2 a = PK ? upk2(acc2[i / 2]) : make_float2(acc[i], acc[i + 1]);
-        const int t = tok0 + hc * HALF + i;  // slice z's partials
-        if (t < nt) out[((size_t)blockIdx.z * nt + t) * od + row_g] = sigma * a.x;
-        if (t + 1 < nt) out[((size_t)blockIdx.z * nt + t + 1) * od + row_g] = sigma * a.y;
+      for (int i = 0; i < CPW; ++i) {
+        const int t = tok0 + cb * CPW + i;  // slice z's partials
+        if (t < nt) out[((size_t)blockIdx.z * nt + t) * od + row_g] = sigma * acc[i];
       }
     }
   }
@@ -633,8 +719,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
-                 : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
   }
 }
 
@@ -681,15 +766,18 @@ int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, in
   if (!make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, (uint64_t)K, (uint64_t)nt, (uint64_t)K * 2, 64,
                    (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return QMM_ELAUNCH;
-  // the block-dot hook writes every group once and needs no slicing
+  // the block-dot hook writes every block once and needs no slicing
   const int S = DOTS ? 1 : gemm_splits(od, K, nt);
   if (S > 1 && !part) return QMM_EWORKSPACE;
   const dim3 grid((unsigned)((od + C::BM - 1) / C::BM), (unsigned)((nt + BN - 1) / BN), (unsigned)S);
   const int limit_ms = stall_ms > 0 ? stall_ms : 4000;
-  gemm_tc_kernel<QT, BN, DOTS><<<grid, C::THREADS, C::SMEM, stream>>>(
-      mw, mx, scl, static_cast<const uint8_t*>(W), S > 1 ? part : out, dots,
-      (int)od, (int)K, (int)nt, (int)gemm_ntp(nt), status, limit_ms, stall_ms > 0 ? 1 : 0);
-  if (cudaGetLastError() != cudaSuccess) return QMM_ELAUNCH;
+  // a programmatic dependent of the kernel before it (the quantizer or the
+  // operand prepass): barrier set-up, TMEM allocation and the tensor-map
+  // prefetch overlap its tail; every load waits for it
+  int rc = launch_ex(gemm_tc_kernel<QT, BN, DOTS>, grid, dim3(C::THREADS), (size_t)C::SMEM, stream, true, mw, mx,
+                     scl, static_cast<const uint8_t*>(W), S > 1 ? part : out, dots, (int)od, (int)K, (int)nt,
+                     (int)gemm_ntp(nt), status, limit_ms, stall_ms > 0 ? 1 : 0);
+  if (rc) return rc;
   if (S > 1) {
     const int64_t n = nt * od;
     int64_t blocks = (n + 255) / 256;
@@ -703,15 +791,9 @@ int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, in
 template <int QT, bool DOTS>
 int launch_qt(const void* W, const __half* xh, const float* scl, float* out, int32_t* dots, float* part, int64_t od,
               int64_t K, int64_t nt, int* status, int stall_ms, cudaStream_t stream) {
-  // the block-dot hook always takes the 128-token tile, so only the product
-  // path instantiates the 64-token one
-  if constexpr (DOTS) {
-    return launch_cfg<QT, 128, true>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
-  } else {
-    if (nt > 64)
-      return launch_cfg<QT, 128, false>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
-    return launch_cfg<QT, 64, false>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
-  }
+  // the block-dot hook runs the same tile choice as the product path
+  if (nt > 64) return launch_cfg<QT, 128, DOTS>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
+  return launch_cfg<QT, 64, DOTS>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
 }
 
 }  // namespace

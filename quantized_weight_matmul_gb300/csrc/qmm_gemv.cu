@@ -108,7 +108,8 @@ template <int QT, int NT, int NW, int R, bool DOTS, bool FUSED>
 __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
     mmvq_stream_kernel(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ x,
                            int8_t* __restrict__ xq, float* __restrict__ xds, float* __restrict__ out,
-                           int32_t* __restrict__ dots, int od, int K, int stages, int* status, int static_w) {
+                           int32_t* __restrict__ dots, int od, int K, int stages, int* status, int static_w,
+                           int limit_ms, int skip_first) {
   using C = GemvCfg<QT, NW, R>;
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t s0 = smem_addr(smem_dyn);
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
   const int nchunks = (g_end - g_begin) * nseg;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Guard g{abort_flag, status, global_ns() + 4000ull * 1000000ull};
+  const Guard g{abort_flag, status, global_ns() + (uint64_t)limit_ms * 1000000ull};
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
@@ -168,8 +169,10 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
           act_issued = true;
         }
         if (!wait_bar(empty0 + 8 * st, ph ^ 1, g)) break;
-        mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE_BYTES);
-        tma_load_2d(sb + st * C::STAGE_BYTES, &tmW, seg * (C::SEG_BYTES / 8), grp * C::CR, full0 + 8 * st);
+        if (!(skip_first && c == 0)) {  // the stall test hook skips the first stage
+          mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE_BYTES);
+          tma_load_2d(sb + st * C::STAGE_BYTES, &tmW, seg * (C::SEG_BYTES / 8), grp * C::CR, full0 + 8 * st);
+        }
         ++issued;
         if (++st == stages) {
           st = 0;
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
       // drain: every copy in flight lands before the CTA exits
       const uint64_t dl = global_ns() + 1000000000ull;
       for (int i = issued - stages; i < issued; ++i) {
-        if (i < 0) continue;
+        if (i < 0 || (skip_first && i == 0)) continue;
         for (uint32_t it = 0; !mbar_try_wait(full0 + 8 * (i % stages), (i / stages) & 1); ++it)
           if ((it & 63u) == 63u && global_ns() > dl) break;
       }
@@ -529,8 +532,9 @@ int launch_stream(const GemvArgs& a, int stages) {
   int grid = nsm > 0 ? nsm : 152;
   if (grid > groups) grid = groups;
   const int iod = (int)a.od, iK = (int)a.K, sw = a.static_w ? 1 : 0;
+  const int stall = stall_ms();
   return launch_ex(kern, dim3(grid), dim3(C::THREADS), (size_t)smem, a.stream, a.pdl, m, a.x, a.xq, a.xds,
-                   a.out, a.dots, iod, iK, stages, a.status, sw);
+                   a.out, a.dots, iod, iK, stages, a.status, sw, stall > 0 ? stall : 4000, stall > 0 ? 1 : 0);
 }
 
 // Staged path: consumer warps and rows per warp by nt -- 16 warps of one row

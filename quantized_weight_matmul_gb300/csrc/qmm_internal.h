@@ -95,6 +95,11 @@ int launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaSt
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) == cudaSuccess ? QMM_OK : QMM_ELAUNCH;
 }
 
+// Test hook (qmm_debug_inject_stall): milliseconds after which the bounded
+// waits of the next launches give up, with the first producer arrival of each
+// CTA skipped so that they do; 0 when off.
+int stall_ms();
+
 // The driver's cuTensorMapEncodeTiled, looked up once (nullptr if absent).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 

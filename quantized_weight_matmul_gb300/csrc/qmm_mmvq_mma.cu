@@ -465,7 +465,7 @@ template <int QT, int NTL, bool X16, bool DOTS>
 __global__ void __launch_bounds__(kThreads, 1)
     mmvq_mma_kernel(const __grid_constant__ CUtensorMap tmW, const int8_t* __restrict__ xq, const float* __restrict__ xds,
                     float* __restrict__ out, int32_t* __restrict__ dots, int od, int K, int nt, int stages,
-                    int* status, int static_w) {
+                    int* status, int static_w, int limit_ms, int skip_first) {
   using C = MC<QT>;
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t s0 = smem_addr(smem_dyn);
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t xbar = red0 + 32;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.bar_off + (2 * stages + 5) * 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Guard gd{abort_flag, status, global_ns() + 4000ull * 1000000ull};
+  const Guard gd{abort_flag, status, global_ns() + (uint64_t)limit_ms * 1000000ull};
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
@@ -508,8 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and bytes past the row's end arrive zero-filled)
       auto issue = [&]() -> bool {
         if (!wait_bar(empty0 + 8 * st, ph ^ 1, gd)) return false;
-        mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE);
-        tma_load_2d(sb + st * C::STAGE, &tmW, seg * (C::SEG / 8), tile * kTileRows, full0 + 8 * st);
+        if (!(skip_first && issued == 0)) {  // the stall test hook skips the first stage
+          mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE);
+          tma_load_2d(sb + st * C::STAGE, &tmW, seg * (C::SEG / 8), tile * kTileRows, full0 + 8 * st);
+        }
         ++issued;
         if (++st == stages) {
           st = 0;
@@ -538,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: every copy in flight lands before the CTA exits
       const uint64_t dl = global_ns() + 1000000000ull;
       for (int i = issued - stages; i < issued; ++i) {
-        if (i < 0) continue;
+        if (i < 0 || (skip_first && i == 0)) continue;
         for (uint32_t k = 0; !mbar_try_wait(full0 + 8 * (i % stages), (i / stages) & 1); ++k)
           if ((k & 63u) == 63u && global_ns() > dl) break;
       }
@@ -593,10 +595,12 @@ int launch_mma_cfg(const void* W, const int8_t* xq, const float* xds, float* out
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return QMM_ELAUNCH;
   const int64_t tiles = (od + kTileRows - 1) / kTileRows;
+  const int stall = stall_ms();
   int grid = nsm > 0 ? nsm : 152;
   if (grid > tiles) grid = (int)tiles;
   return launch_ex(kern, dim3(grid), dim3(kThreads), (size_t)p.total + 1024, stream, pdl, m, xq, xds, out, dots,
-                   (int)od, (int)K, (int)nt, p.stages, status, static_w ? 1 : 0);
+                   (int)od, (int)K, (int)nt, p.stages, status, static_w ? 1 : 0, stall > 0 ? stall : 4000,
+                   stall > 0 ? 1 : 0);
 }
 
 template <int QT, int NTL, bool DOTS>

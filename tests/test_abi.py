@@ -30,6 +30,7 @@ def test_weight_and_activation_sizes():
     assert qmm.qmm_weight_bytes(qmm.Q4_K, 16, 300) == 0
     assert qmm.qmm_weight_bytes(7, 16, 256) == 0
     assert qmm.qmm_xq_bytes(3, 512) == 1536
+    assert qmm.qmm_q8_1_bytes(3, 512) == 1536 and qmm.qmm_q8_1_bytes(-1, 512) == 0
     assert qmm.qmm_xds_bytes(3, 512) == 3 * 16 * 8
     assert qmm.qmm_gemv_max_nt() == 16
     assert qmm.qmm_matmul_workspace_bytes(qmm.Q4_K, 4096, 4096, 8) == 0

@@ -10,6 +10,7 @@ largest on a deterministic row sample).
 import numpy as np
 import pytest
 
+import brute
 import quantized_weight_matmul_gb300 as qmm
 from gpu_helpers import assert_close_rows, dev, ora, oracle_rows, row_sample, threads
 from quantized_weight_matmul_gb300 import synth
@@ -113,16 +114,77 @@ def test_gemv_q6k_block_dots_bit_exact(od, K, nt):
     assert np.array_equal(d.cpu().numpy(), ora().block_dots(Q6_K, W, xq, od))
 
 
+def _tc_dots_expected(qtype, W, xq, od):
+    """What the tensor-core kernel's accumulator holds per 32-value block, from
+    the oracle's exact block dots and the scales decoded by the separate numpy
+    restatement: Q4_K sc_j * D_j; Q6_K sc_2b * D_2b + sc_2b+1 * D_2b+1; zero
+    for a super-block whose d is zero (the kernel folds no scale there)."""
+    D = ora().block_dots(qtype, W, xq, od).astype(np.int64)
+    nt, K = xq.shape
+    nsb = K // 256
+    if qtype == Q4_K:
+        blocks = W.reshape(od, nsb, 144)
+        sc, _ = brute.q4k_codes(blocks)
+        dz = brute.f16_field(blocks, 0) == 0
+        sc = np.where(dz[..., None], 0, sc).reshape(od, nsb * 8)
+        return D * sc[None]
+    blocks = W.reshape(od, nsb, 210)
+    sc = brute.q6k_scales(blocks)
+    dz = brute.f16_field(blocks, 208) == 0
+    sc = np.where(dz[..., None], 0, sc).reshape(od, nsb * 16)
+    return (D * sc[None]).reshape(nt, od, K // 32, 2).sum(-1)
+
+
 @pytest.mark.parametrize("qtype,od,K,nt", [(Q4_K, 300, 512, 70), (Q4_K, 129, 1024, 200),
-                                           (Q4_K, 128, 256, 1), (Q6_K, 300, 2048, 70),
-                                           (Q6_K, 130, 4096, 131)])
+                                           (Q4_K, 128, 256, 1), (Q4_K, 257, 2048, 64),
+                                           (Q6_K, 300, 2048, 70), (Q6_K, 130, 4096, 131),
+                                           (Q6_K, 200, 2048, 33), (Q6_K, 129, 2048, 64)])
 def test_gemm_block_dots_bit_exact(qtype, od, K, nt):
+    """The tensor-core kernel's exact integer sums, as the product kernel
+    forms them (scale folded into the weight operand; the 64-token tile up to
+    64 tokens, the 128-token tile above), against the oracle's block dots."""
     W, x = _case(qtype, od, K, nt, seed=od + nt)
     xq, xds = ora().quantize_q8_1(x)
     d = qmm.block_dots(qtype, dev(W, torch), dev(xq, torch), dev(xds, torch), od, path=1)
     torch.cuda.synchronize()
     assert qmm.qmm_sync_status(0) == qmm.QMM_OK
-    assert np.array_equal(d.cpu().numpy(), ora().block_dots(qtype, W, xq, od))
+    assert np.array_equal(d.cpu().numpy().astype(np.int64), _tc_dots_expected(qtype, W, xq, od))
+
+
+@pytest.mark.parametrize("qtype,nt", [(Q4_K, 40), (Q4_K, 100), (Q6_K, 40), (Q6_K, 100)])
+def test_gemm_block_dots_extremes(qtype, nt):
+    """Largest sums the folded operands can produce, where an inexact f32
+    accumulation would show: Q4_K sc = 63 with all nibbles 15, Q6_K q = 0
+    (q - 32 = -32) with scale -128 and q = 63 with scale 127, against codes of
+    +-127 (|sum| up to 32*32*128*127 < 2^24), plus super-blocks with d = 0
+    and mixed signs."""
+    od, K = 200, 2048
+    W, x = _case(qtype, od, K, nt, seed=5)
+    nsb = K // 256
+    if qtype == Q4_K:
+        Wb = W.reshape(od, nsb, 144).copy()
+        Wb[0::3, :, 4:16] = brute.pack_q4k_codes([63] * 8, [63] * 8)  # sc = m = 63
+        Wb[0::3, :, 16:] = 0xFF                                         # nibbles 15
+        Wb[1::7, 1, 0:2] = 0                                            # d = 0
+    else:
+        Wb = W.reshape(od, nsb, 210).copy()
+        Wb[0::3, :, 0:192] = 0                                          # q = 0
+        Wb[0::3, :, 192:208] = 0x80                                     # scale -128
+        Wb[1::3, :, 0:192] = 0xFF                                       # q = 63
+        Wb[1::3, :, 192:208] = 0x7F                                     # scale 127
+        Wb[2::7, 1, 208:210] = 0                                        # d = 0
+    W = Wb.reshape(od, -1)
+    x = np.where(np.arange(K)[None, :] % 64 < 32, 1.0, -1.0).astype(np.float32) * np.ones((nt, 1), np.float32)
+    x[1::2] *= -1.0
+    x[2, 96:128] = 0.0
+    xq, xds = ora().quantize_q8_1(x)
+    assert np.abs(xq).max() == 127
+    d = qmm.block_dots(qtype, dev(W, torch), dev(xq, torch), dev(xds, torch), od, path=1)
+    torch.cuda.synchronize()
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+    want = _tc_dots_expected(qtype, W, xq, od)
+    assert np.abs(want).max() > (2 ** 23 if qtype == Q6_K else 2 ** 19)
+    assert np.array_equal(d.cpu().numpy().astype(np.int64), want)
 
 
 @pytest.mark.parametrize("qtype,od,K,nt", [(Q4_K, 256, 512, 1), (Q4_K, 300, 768, 3), (Q4_K, 1000, 4096, 8),
@@ -371,3 +433,36 @@ def test_errors_and_bounded_wait():
     got = qmm.gemm(Q4_K, Wd, xq, xds, 256).cpu().numpy()
     assert qmm.qmm_sync_status(st) == qmm.QMM_OK
     assert_close_rows(got, ref, "after timeout")
+
+
+@pytest.mark.parametrize("route,nt", [("fused", 1), ("fused", 3), ("staged", 2), ("mma", 8), ("mma", 13)])
+def test_mmvq_bounded_wait(route, nt):
+    """The MMVQ kernels' bounded waits: with the stall hook on, a skipped
+    producer arrival makes their waits run out; qmm_sync_status reports
+    QMM_ETIMEOUT, and the next call on the same context matches the oracle.
+    Routes: the fused quantize + dp4a kernel (qmm_matmul, decode shapes), the
+    staged dp4a kernel (qmm_gemv, few tokens), the warp-MMA kernel (qmm_gemv,
+    5..16 tokens)."""
+    od, K = 300, 4096
+    W, x = _case(Q4_K, od, K, nt, outliers=True, seed=nt)
+    Wd, xd = dev(W, torch), dev(x, torch)
+    xq, xds = qmm.quantize_q8_1(xd)
+    st = torch.cuda.current_stream().cuda_stream
+    if route == "fused":
+        assert qmm.qmm_matmul_path(Q4_K, od, K, nt) == qmm.QMM_PATH_FUSED_MMVQ
+        run = lambda: qmm.matmul(Q4_K, Wd, xd, od)
+        ref = ora().matmul(Q4_K, W, x, od, nthreads=threads())
+    else:
+        run = lambda: qmm.gemv(Q4_K, Wd, xq, xds, od)
+        oq, ods = ora().quantize_q8_1(x)
+        ref = ora().matmul_q8_1(Q4_K, W, oq, ods, od, nthreads=threads())
+    assert qmm.qmm_sync_status(st) == qmm.QMM_OK
+    assert qmm.qmm_debug_inject_stall(1, 200) == qmm.QMM_OK
+    try:
+        run()
+        assert qmm.qmm_sync_status(st) == qmm.QMM_ETIMEOUT
+    finally:
+        qmm.qmm_debug_inject_stall(0, 0)
+    got = run().cpu().numpy()
+    assert qmm.qmm_sync_status(st) == qmm.QMM_OK
+    assert_close_rows(got, ref, f"{route} nt={nt} after timeout")
