@@ -66,10 +66,10 @@ NCOPIES = 16
 # ncu capture of the fused quantize + MMVQ kernel (nt = 1, 11008 x 4096): dram
 # read + write bytes per launch, and the hash of qmm_gemv.cu it was taken on.
 # Reported as roofline.traffic only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha1": "2b6387032060324d16d3758decfceb84e6c26c5e", "bytes_per_launch": 25408256}
+NCU_TRAFFIC = {"source_sha1": "e8269341b0f9c83e84d35a4c6d5cf8ee33fa6538", "bytes_per_launch": 25408768}
 # The same for the tensor-core GEMM (Q4_K 14336 x 4096, nt = 512; prepass and
 # GEMM kernel launches added), keyed on qmm_gemm_tc.cu.
-NCU_TRAFFIC_GEMM = {"source_sha1": None, "bytes_per_launch": None}
+NCU_TRAFFIC_GEMM = {"source_sha1": "f7b301c8dc44372d334e667783df790db643cadf", "bytes_per_launch": 2639616 + 38114816 + 307456}
 
 # The cases of the per_nt array: (qtype name, od, K, nt values).
 PER_NT = [("Q4_K", 4096, 4096, (1, 2, 4, 8, 16, 128, 512, 2048)),
