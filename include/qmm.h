@@ -150,6 +150,9 @@ int qmm_gemv(int qtype, const void *W, const int8_t *xq, const float *xds, float
  * `workspace` (device, 16-byte aligned, >= qmm_gemm_workspace_bytes) holds
  * an f16 copy of xq and the scale planes written by a prepass on `stream`;
  * its contents need not be preserved between calls.  out is overwritten.
+ * Any K % 256 == 0: rows whose pitch is not a multiple of 16 bytes (Q6_K with
+ * K % 2048 != 0), which a TMA tensor map cannot describe, are staged row by
+ * row as 16-byte-aligned windows around each block.
  * When the 128-row x token tiles are fewer than the GPU's SMs, K is split
  * into up to 8 slices of whole super-blocks computed by separate CTAs; their
  * fp32 partial sums (in the workspace) are added in a fixed order, so
@@ -201,8 +204,9 @@ int qmm_gemm_builtin_workspace(int qtype, const void *W, const int8_t *xq, const
  *     shapes): one fused kernel quantizes x to q8_1 inside the dp4a MMVQ
  *     kernel (bit-identical codes) and writes xq / xds and out;
  *   - other nt <= 8: qmm_quantize_q8_1 into xq / xds, then qmm_gemv;
- *   - otherwise: qmm_quantize_q8_1 (which also writes the GEMM workspace),
- *     then the tensor-core GEMM of qmm_gemm.
+ *   - otherwise, and for every nt when the MMVQ kernels cannot stage the
+ *     rows (Q6_K with K % 2048 != 0): qmm_quantize_q8_1 (which also writes
+ *     the GEMM workspace), then the tensor-core GEMM of qmm_gemm.
  * The matmul kernels are launched as programmatic dependents of the kernel
  * before them and wait for it before reading anything it may write.  With
  * QMM_FLAG_STATIC_WEIGHTS the caller promises that W is not written by any

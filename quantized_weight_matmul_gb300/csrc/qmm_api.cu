@@ -79,9 +79,13 @@ int matmul_route(int qtype, int64_t nt, int64_t K) {
 
 // Every refusal of the tensor-core route, checked before any device work is
 // enqueued; on success *status is the device status word.
-// The tensor-core route's own shape rule (host only): the Q6_K weight map
-// needs a 16-byte row pitch, which 210-byte blocks give every 8 blocks.
-int gemm_shape(int qtype, int64_t K) { return qtype == QMM_Q6_K && K % 2048 ? QMM_EINVAL_SHAPE : QMM_OK; }
+// The tensor-core route's own shape rule (host only), beyond check_shape:
+// none at present (rows of any pitch are staged, see qmm_gemm_tc.cu).
+int gemm_shape(int qtype, int64_t K) {
+  (void)qtype;
+  (void)K;
+  return QMM_OK;
+}
 
 int gemm_check(int qtype, int64_t od, int64_t K, int64_t nt, const void* ws, size_t ws_bytes, int** status) {
   if (ws_bytes < gemm_ws(od, K, nt)) return QMM_EWORKSPACE;
@@ -144,9 +148,7 @@ int qmm_matmul_path(int qtype, int64_t od, int64_t K, int64_t nt) {
   if (!valid_qtype(qtype)) return QMM_EINVAL_QTYPE;
   int rc = check_shape(od, K, nt);
   if (rc) return rc;
-  const int path = matmul_route(qtype, nt, K);
-  if (path == QMM_PATH_MMQ && qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
-  return path;
+  return matmul_route(qtype, nt, K);
 }
 
 int qmm_gemv_max_nt(void) { return kMmaMaxNt; }

@@ -89,6 +89,7 @@ struct Cfg {
   // the 2-byte-aligned 210-byte block; 240 rather than 224 bytes, so that a
   // warp's 32-bit loads of 32 rows hit 8 bank offsets instead of 4)
   static constexpr int RAW_ROW = QT == kQ4 ? 144 : 240;
+  static constexpr int BLK = QT == kQ4 ? kQ4KBytes : kQ6KBytes;
   static constexpr int RAW_BYTES = BM * RAW_ROW;
   static constexpr bool MINT = QT == kQ4;                // Q4_K min term
   static constexpr int MINB_BYTES = MINT ? BN * 64 : 0;  // 4 chunks x BN tokens x 8 bf16
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const float* __restrict__ scl, const uint8_t* __restrict__ W, float* __restrict__ out,
                    int32_t* __restrict__ dots, int od, int K, int nt, int ntp, int* status, int limit_ms,
-                   int skip_first_weight_load) {
+                   int skip_first_weight_load, int row_copy) {
   using C = Cfg<QT, BN>;
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t s0 = smem_addr(smem_dyn);
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmW);
+    if (!row_copy) prefetch_tmap(&tmW);
     prefetch_tmap(&tmX);
   }
   if (warp == 1) {
@@ -313,26 +314,74 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
     regs_release<C::REG_CTL>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      // everything loaded below may be written by the preceding kernel
-      griddep_wait();
-      int raw_issued = 0, b_issued = 0;
-      bool ok = true;
-      for (int b = 0; b < nsb && ok; ++b) {
-        const int rs = b % C::RS;
-        if (!gwait(bars.raw_empty(rs), ((b / C::RS) & 1) ^ 1, g)) break;
-        if (!(skip_first_weight_load && b == 0)) {
-          mbar_arrive_expect_tx(bars.raw_full(rs), C::RAW_BYTES + (MIN ? C::MINB_BYTES : 0));
-          const int x = QT == kQ4 ? (b + b_off) * kQ4KBytes : ((b + b_off) * kQ6KBytes) & ~15;
-          tma_load_2d(raw_s + rs * C::RAW_BYTES, &tmW, x, row0, bars.raw_full(rs));
-          if (MIN) {
-#pragma unroll
-            for (int kc = 0; kc < 4; ++kc)
-              bulk_load(minb_s + rs * C::MINB_BYTES + kc * BN * 16,
-                        smin + (((size_t)(b + b_off) * 4 + kc) * ntp + tok0) * 16, BN * 16, bars.raw_full(rs));
+    // Lane 0 waits for free stages and issues the copies.  Raw weights come
+    // as one 2-D TMA box of 128 rows, or -- when the row pitch is not a
+    // multiple of 16 bytes (Q6_K with K % 2048 != 0), which a tensor map
+    // cannot describe -- as one bulk copy per row of the 16-byte-aligned
+    // window around the row's 210-byte block, issued by all 32 lanes.
+    const size_t row_bytes = (size_t)nsb_all * (QT == kQ4 ? kQ4KBytes : kQ6KBytes);
+    const size_t w_bytes = (size_t)od * row_bytes;
+    // everything loaded below may be written by the preceding kernel
+    griddep_wait();
+    int raw_issued = 0, b_issued = 0;
+    bool ok = true;
+    for (int b = 0; b < nsb && ok; ++b) {
+      const int rs = b % C::RS;
+      bool okw = true;
+      if (lane == 0) okw = gwait(bars.raw_empty(rs), ((b / C::RS) & 1) ^ 1, g);
+      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+      if (!(skip_first_weight_load && b == 0)) {
+        if (!row_copy) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bars.raw_full(rs), C::RAW_BYTES + (MIN ? C::MINB_BYTES : 0));
+            const int x = QT == kQ4 ? (b + b_off) * kQ4KBytes : ((b + b_off) * kQ6KBytes) & ~15;
+            tma_load_2d(raw_s + rs * C::RAW_BYTES, &tmW, x, row0, bars.raw_full(rs));
           }
+        } else {
+          // rows lane + 32i: window [start & ~15, (end + 15) & ~15) of the
+          // block's bytes [start, end), capped at the matrix's last 16-byte
+          // boundary; the at most 14 bytes past it (last row only) are copied
+          // with ordinary loads before the barrier is armed
+          uint32_t bytes = 0;
+          size_t a0[4], a1[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = lane + 32 * i;
+            a0[i] = a1[i] = 0;
+            if (row0 + r >= od) continue;
+            const size_t start = (size_t)(row0 + r) * row_bytes + (size_t)(b + b_off) * C::BLK;
+            const size_t end = start + C::BLK;
+            a0[i] = start & ~(size_t)15;
+            a1[i] = (end + 15) & ~(size_t)15;
+            const size_t cap = w_bytes & ~(size_t)15;
+            if (a1[i] > cap) {
+              uint8_t* dst = smem + C::RAW_OFF + rs * C::RAW_BYTES + r * C::RAW_ROW;
+              for (size_t o = cap; o < end; o += 2)
+                *reinterpret_cast<uint16_t*>(dst + (o - a0[i])) = __ldg(reinterpret_cast<const uint16_t*>(W + o));
+              a1[i] = cap;
+            }
+            bytes += (uint32_t)(a1[i] - a0[i]);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_expect_tx(bars.raw_full(rs), bytes + (MIN ? C::MINB_BYTES : 0));
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (a1[i] > a0[i])
+              bulk_load(raw_s + rs * C::RAW_BYTES + (lane + 32 * i) * C::RAW_ROW, W + a0[i], (uint32_t)(a1[i] - a0[i]),
+                        bars.raw_full(rs));
         }
-        ++raw_issued;
+        if (MIN && lane == 0) {
+#pragma unroll
+          for (int kc = 0; kc < 4; ++kc)
+            bulk_load(minb_s + rs * C::MINB_BYTES + kc * BN * 16,
+                      smin + (((size_t)(b + b_off) * 4 + kc) * ntp + tok0) * 16, BN * 16, bars.raw_full(rs));
+        }
+      }
+      ++raw_issued;
+      if (lane == 0) {
         for (int s = 0; s < 4; ++s) {
           const int gs = 4 * b + s, bs = gs % C::BS;
           if (!gwait(bars.b_empty(bs), ((gs / C::BS) & 1) ^ 1, g)) {
@@ -345,7 +394,10 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
           ++b_issued;
         }
       }
-      // drain: every copy still in flight lands before the CTA may exit
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    // drain: every copy still in flight lands before the CTA may exit
+    if (lane == 0) {
       const uint64_t dl = global_ns() + 1000000000ull;
       for (int i = raw_issued - C::RS; i < raw_issued; ++i)
         if (i >= 0 && !(skip_first_weight_load && i == 0))
@@ -490,7 +542,9 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
       if constexpr (QT == kQ4) {
         hdr = *reinterpret_cast<const uint4*>(row);
       } else {
-        blk_off = ((b + b_off) * kQ6KBytes) & 15;
+        // the block's offset in its row's window: the same for every row when
+        // the row pitch is a multiple of 16 (one TMA box), per row otherwise
+        blk_off = (int)(((size_t)(row0 + r) * ((size_t)nsb_all * kQ6KBytes) + (size_t)(b + b_off) * kQ6KBytes) & 15);
         d6 = *reinterpret_cast<const uint16_t*>(row + blk_off + 208);
       }
       // a rolled loop: the unpack, epilogue and MMA roles run different code
@@ -759,9 +813,12 @@ int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, in
   static PerDevice<bool> attr_done;
   if (int rc = smem_attr_once(gemm_tc_kernel<QT, BN, DOTS>, C::SMEM, attr_done, dev)) return rc;
   const uint64_t row_bytes = (uint64_t)(K / 256) * (QT == kQ4 ? kQ4KBytes : kQ6KBytes);
-  CUtensorMap mw, mx;
-  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, (uint64_t)od, row_bytes,
-                   (uint32_t)C::RAW_ROW, (uint32_t)C::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+  // a tensor map needs a row pitch that is a multiple of 16 bytes; other
+  // pitches (Q6_K with K % 2048 != 0) are copied row by row instead
+  const int row_copy = row_bytes % 16 ? 1 : 0;
+  CUtensorMap mw = {}, mx;
+  if (!row_copy && !make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, row_bytes, (uint64_t)od, row_bytes,
+                                (uint32_t)C::RAW_ROW, (uint32_t)C::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
     return QMM_ELAUNCH;
   if (!make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, (uint64_t)K, (uint64_t)nt, (uint64_t)K * 2, 64,
                    (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -776,7 +833,7 @@ int launch_cfg(const void* W, const __half* xh, const float* scl, float* out, in
   // prefetch overlap its tail; every load waits for it
   int rc = launch_ex(gemm_tc_kernel<QT, BN, DOTS>, grid, dim3(C::THREADS), (size_t)C::SMEM, stream, true, mw, mx,
                      scl, static_cast<const uint8_t*>(W), S > 1 ? part : out, dots, (int)od, (int)K, (int)nt,
-                     (int)gemm_ntp(nt), status, limit_ms, stall_ms > 0 ? 1 : 0);
+                     (int)gemm_ntp(nt), status, limit_ms, stall_ms > 0 ? 1 : 0, row_copy);
   if (rc) return rc;
   if (S > 1) {
     const int64_t n = nt * od;
@@ -804,7 +861,6 @@ int launch_gemm_tc(int qtype, const void* W, const __half* xh, const float* scl,
     return dots ? launch_qt<kQ4, true>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream)
                 : launch_qt<kQ4, false>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
   if (qtype == QMM_Q6_K) {
-    if (K % 2048) return QMM_EINVAL_SHAPE;  // 16-byte row pitch for the TMA weight map
     return dots ? launch_qt<kQ6, true>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream)
                 : launch_qt<kQ6, false>(W, xh, scl, out, dots, part, od, K, nt, status, stall_ms, stream);
   }

@@ -78,7 +78,8 @@ def test_matmul_route_query():
     while the activations leave room for its weight ring, quantize + the
     warp-MMA MMVQ from 5 tokens (Q4_K) or 2 (Q6_K) up to 16 where it fits,
     quantize + the dp4a MMVQ for the other nt <= 8, the tensor-core GEMM
-    beyond; workspace is needed exactly on the GEMM route."""
+    beyond and for Q6_K rows the MMVQ kernels cannot stage (K % 2048 != 0);
+    workspace is needed exactly on the GEMM route."""
     Q4, Q6 = qmm.Q4_K, qmm.Q6_K
     F, V, G = qmm.QMM_PATH_FUSED_MMVQ, qmm.QMM_PATH_MMVQ, qmm.QMM_PATH_MMQ
     cases = [((Q4, 4096, 4096, 1), F), ((Q4, 11008, 4096, 1), F), ((Q4, 256, 512, 4), F),
@@ -87,11 +88,14 @@ def test_matmul_route_query():
              ((Q4, 14336, 16384, 3), V), ((Q4, 4096, 4096, 9), V), ((Q4, 4096, 4096, 16), V),
              ((Q4, 4096, 4096, 17), G), ((Q4, 4096, 4096, 512), G), ((Q6, 4096, 4096, 1), F),
              ((Q6, 32000, 4096, 2), V), ((Q6, 4096, 4096, 8), V), ((Q6, 4096, 4096, 9), V),
-             ((Q6, 4096, 4096, 17), G), ((Q6, 32000, 4096, 80), G)]
+             ((Q6, 4096, 4096, 17), G), ((Q6, 32000, 4096, 80), G),
+             # Q6_K rows whose pitch is not a multiple of 16 bytes (K % 2048 != 0)
+             # are staged row by row: only the tensor-core route takes them
+             ((Q6, 4096, 768, 32), G), ((Q6, 4096, 11008, 1), G), ((Q6, 4096, 2304, 8), G),
+             ((Q6, 300, 256, 64), G)]
     for args, path in cases:
         assert qmm.qmm_matmul_path(*args) == path, args
         assert (qmm.qmm_matmul_workspace_bytes(*args) > 0) == (path == qmm.QMM_PATH_MMQ), args
-    assert qmm.qmm_matmul_path(Q6, 4096, 768, 32) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_matmul_path(Q4, 4096, 300, 1) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_matmul_path(Q4, 4096, 4096, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_matmul_path(3, 4096, 4096, 1) == qmm.QMM_EINVAL_QTYPE

@@ -415,11 +415,10 @@ def test_errors_and_bounded_wait():
                         ws.data_ptr(), 64, st) == qmm.QMM_EINVAL_QTYPE
     assert qmm.qmm_gemv(Q4_K, Wd.data_ptr() + 8, xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 8,
                         st) == qmm.QMM_EALIGN
-    # Q6_K needs a 16-byte row pitch for the tensor-core path (K % 2048 == 0)
-    assert qmm.qmm_gemm_workspace_bytes(Q6_K, 256, 512, 16) > 0
-    ws = qmm.workspace(qmm.qmm_gemm_workspace_bytes(Q6_K, 256, 512, 16), "cuda")
-    assert qmm.qmm_gemm(Q6_K, Wd.data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 16,
-                        ws.data_ptr(), ws.numel(), st) == qmm.QMM_EINVAL_SHAPE
+    # the MMVQ kernels stage Q6_K rows by TMA, which needs a 16-byte row pitch
+    # (K % 2048 == 0); other K take the tensor-core route
+    assert qmm.qmm_gemv(Q6_K, Wd.data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 16,
+                        st) == qmm.QMM_EINVAL_SHAPE
     # bounded wait: a skipped producer arrival makes the waits give up and report
     assert qmm.qmm_sync_status(st) == qmm.QMM_OK
     assert qmm.qmm_debug_inject_stall(1, 200) == qmm.QMM_OK
@@ -466,3 +465,29 @@ def test_mmvq_bounded_wait(route, nt):
     got = run().cpu().numpy()
     assert qmm.qmm_sync_status(st) == qmm.QMM_OK
     assert_close_rows(got, ref, f"{route} nt={nt} after timeout")
+
+
+@pytest.mark.parametrize("od,K,nt", [(300, 11008, 1), (300, 11008, 8), (300, 11008, 64), (257, 2304, 1),
+                                     (257, 2304, 8), (257, 2304, 64), (129, 256, 70), (64, 768, 130)])
+def test_q6k_any_k(od, K, nt):
+    """Q6_K rows whose pitch (210*K/256 bytes) is not a multiple of 16 -- K %
+    2048 != 0, e.g. K = 11008, a Llama-7B FFN-down width -- cannot be a TMA
+    tensor map; the tensor-core GEMM stages them row by row (16-byte-aligned
+    windows, the last row's tail by ordinary loads) for every nt.  Outputs
+    within tolerance, q8_1 bit-exact, the exact folded block sums, and a
+    deterministic repeat."""
+    assert qmm.qmm_matmul_path(Q6_K, od, K, nt) == qmm.QMM_PATH_MMQ
+    W, x = _case(Q6_K, od, K, nt, outliers=True, seed=K + nt)
+    Wd, xd = dev(W, torch), dev(x, torch)
+    out, xq, xds = qmm.matmul(Q6_K, Wd, xd, od, return_q8=True)
+    oq, ods = ora().quantize_q8_1(x)
+    assert np.array_equal(xq.cpu().numpy(), oq)
+    ref = ora().matmul_q8_1(Q6_K, W, oq, ods, od, nthreads=threads())
+    got = out.cpu().numpy()
+    assert_close_rows(got, ref, f"q6k {od}x{K} nt={nt}")
+    again = qmm.matmul(Q6_K, Wd, xd, od).cpu().numpy()
+    assert np.array_equal(again.view(np.uint32), got.view(np.uint32))
+    d = qmm.block_dots(Q6_K, Wd, dev(oq, torch), dev(ods, torch), od, path=1)
+    torch.cuda.synchronize()
+    assert qmm.qmm_sync_status(0) == qmm.QMM_OK
+    assert np.array_equal(d.cpu().numpy().astype(np.int64), _tc_dots_expected(Q6_K, W, oq, od))

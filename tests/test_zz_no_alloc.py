@@ -31,10 +31,8 @@ def test_size_limit_is_refused_before_any_device_work():
     assert qmm.qmm_gemm_workspace_bytes(Q4_K, 4096, 4096, 832) == qmm.QMM_BUILTIN_WORKSPACE_BYTES
     assert qmm.qmm_gemm_builtin_workspace(Q4_K, p, p, p, p, 4096, 4096, 833, 0) == qmm.QMM_EWORKSPACE
     assert qmm.qmm_gemm_builtin_workspace(Q4_K, p, p, p, p, 4096, 300, 8, 0) == qmm.QMM_EINVAL_SHAPE
-    # a Q6_K K the tensor-core route refuses is refused before the call clears
-    # the padding entries of the shared array
-    assert qmm.qmm_gemm_workspace_bytes(Q6_K, 4096, 512, 8) <= qmm.QMM_BUILTIN_WORKSPACE_BYTES
-    assert qmm.qmm_gemm_builtin_workspace(Q6_K, p, p, p, p, 4096, 512, 8, 0) == qmm.QMM_EINVAL_SHAPE
+    # refusals of a misaligned pointer also come before any device work
+    assert qmm.qmm_gemm_builtin_workspace(Q6_K, p, p + 2, p, p, 4096, 512, 8, 0) == qmm.QMM_EALIGN
     assert qmm.qmm_gemm_builtin_workspace(Q4_K, 0, p, p, p, 4096, 4096, 8, 0) == qmm.QMM_ENULL
     assert qmm.qmm_gemm_builtin_workspace(9, p, p, p, p, 4096, 4096, 8, 0) == qmm.QMM_EINVAL_QTYPE
 
