@@ -126,9 +126,9 @@ int qmm_quantize_q8_1(const float *x, int64_t nt, int64_t K, int8_t *xq, float *
  * block meet all nt tokens while it is on chip, so the weight traffic does not
  * grow with nt.  Q4_K: per 32-value sub-block j the integer dot
  * D = sum(nibble * q) is rescaled as d*sc_j*dx*D - dmin*m_j*s.  Q6_K: per
- * 16-value group g, D = sum((q6 - 32) * q) is rescaled as d*sc_g*dx*D; Q6_K
- * needs K % 2048 == 0 (QMM_EINVAL_SHAPE otherwise: the 210-byte blocks give a
- * 16-byte row pitch only every 8 blocks).  Few tokens (nt <= 4 for Q4_K,
+ * 16-value group g, D = sum((q6 - 32) * q) is rescaled as d*sc_g*dx*D.  Rows
+ * whose pitch is not a multiple of 16 bytes (Q6_K with K % 2048 != 0) are
+ * staged row by row as 16-byte-aligned windows.  Few tokens (nt <= 4 for Q4_K,
  * nt = 1 for Q6_K) take the dp4a kernel, more tokens the warp-level
  * tensor-core MMA kernel (mma.sync on exact small-integer f16 operands).
  * QMM_ESMEM when the nt x K activations do not fit the chosen kernel's shared
@@ -204,9 +204,8 @@ int qmm_gemm_builtin_workspace(int qtype, const void *W, const int8_t *xq, const
  *     shapes): one fused kernel quantizes x to q8_1 inside the dp4a MMVQ
  *     kernel (bit-identical codes) and writes xq / xds and out;
  *   - other nt <= 8: qmm_quantize_q8_1 into xq / xds, then qmm_gemv;
- *   - otherwise, and for every nt when the MMVQ kernels cannot stage the
- *     rows (Q6_K with K % 2048 != 0): qmm_quantize_q8_1 (which also writes
- *     the GEMM workspace), then the tensor-core GEMM of qmm_gemm.
+ *   - otherwise: qmm_quantize_q8_1 (which also writes the GEMM workspace),
+ *     then the tensor-core GEMM of qmm_gemm.
  * The matmul kernels are launched as programmatic dependents of the kernel
  * before them and wait for it before reading anything it may write.  With
  * QMM_FLAG_STATIC_WEIGHTS the caller promises that W is not written by any
@@ -224,7 +223,7 @@ int qmm_matmul(int qtype, const void *W, const float *x, int8_t *xq, float *xds,
  * as a matmul path but written out before any scaling.
  *   Q4_K: dots[t][r][j] = sum_{i<32} nibble[r][32j+i] * xq[t][32j+i], j < K/32
  *   Q6_K: dots[t][r][g] = sum_{i<16} (q6[r][16g+i] - 32) * xq[t][16g+i], g < K/16
- * path 0: the dp4a MMVQ dot code, nt <= 8 (Q6_K: K % 2048 == 0).
+ * path 0: the dp4a MMVQ dot code, nt <= 8.
  * path 1: the tensor-core (qmm_gemm) dot code with the same tile choice and
  *         weight operands as the product kernel, which carry the integer
  *         group scales, so the sums come out scaled, one per 32-value block:
@@ -234,7 +233,7 @@ int qmm_matmul(int qtype, const void *W, const float *x, int8_t *xq, float *xds,
  *                 int8 scales of the block's two 16-value groups), b < K/32;
  *         both 0 for a super-block whose d is 0.  Needs xds (for the
  *         prepass) and a workspace of qmm_gemm_workspace_bytes.
- * path 2: the warp-MMA MMVQ dot code, nt <= 16 (Q6_K: K % 2048 == 0); needs
+ * path 2: the warp-MMA MMVQ dot code, nt <= 16; needs
  *         xds; QMM_ESMEM where the activations do not fit its shared memory.
  * dots is a device buffer of nt*od*ng int32: ng = K/32, except K/16 for
  * Q6_K on paths 0 and 2.

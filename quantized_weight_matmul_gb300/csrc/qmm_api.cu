@@ -169,7 +169,6 @@ int qmm_gemv(int qtype, const void* W, const int8_t* xq, const float* xds, float
   int rc = check_shape(od, K, nt);
   if (rc) return rc;
   if (nt > kMmaMaxNt) return QMM_EINVAL_SHAPE;
-  if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;  // 16-byte TMA row pitch
   if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
   rc = check_device();
   if (rc) return rc;
@@ -245,7 +244,6 @@ int qmm_debug_block_dots(int qtype, const void* W, const int8_t* xq, const float
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (path == 0) {
     if (nt > 8) return QMM_EINVAL_SHAPE;
-    if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
     if (!xds) return QMM_ENULL;
     int* status = nullptr;
     rc = status_ptr(&status);
@@ -254,7 +252,6 @@ int qmm_debug_block_dots(int qtype, const void* W, const int8_t* xq, const float
   }
   if (path == 2) {
     if (nt > kMmaMaxNt) return QMM_EINVAL_SHAPE;
-    if (qtype == QMM_Q6_K && K % 2048) return QMM_EINVAL_SHAPE;
     if (!xds) return QMM_ENULL;
     if (!aligned16(xds)) return QMM_EALIGN;
     int* status = nullptr;

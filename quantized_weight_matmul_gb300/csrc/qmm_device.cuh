@@ -303,6 +303,29 @@ __device__ __forceinline__ void load_words_even(const uint8_t* base, int off, ui
   }
 }
 
+// Rows whose pitch is not a multiple of 16 bytes (Q6_K with K % 2048 != 0)
+// cannot be described by a TMA tensor map; they are staged row by row as
+// the 16-byte-aligned window [start & ~15, (end + 15) & ~15) around the bytes
+// [start, end) of a matrix of `total` bytes.  The window is cut at the
+// matrix's last 16-byte boundary so that no copy reads past the matrix; the
+// (even, at most 14) bytes past that boundary are copied here with ordinary
+// 2-byte loads into their place in `dst`, the window's first byte.  Returns
+// the byte range left to the bulk copy (empty when a1 <= a0).
+struct RowWindow {
+  size_t a0, a1;
+};
+__device__ __forceinline__ RowWindow stage_row_window(size_t start, size_t end, size_t total, uint8_t* dst,
+                                                      const uint8_t* W) {
+  RowWindow w{start & ~(size_t)15, (end + 15) & ~(size_t)15};
+  const size_t cap = total & ~(size_t)15;
+  if (w.a1 > cap) {
+    for (size_t o = cap > w.a0 ? cap : w.a0; o < end; o += 2)
+      *reinterpret_cast<uint16_t*>(dst + (o - w.a0)) = __ldg(reinterpret_cast<const uint16_t*>(W + o));
+    w.a1 = cap;
+  }
+  return w;
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -50,6 +50,13 @@ constexpr int kQ4 = 0, kQ6 = 1;
 constexpr int kSegSB = 8;  // super-blocks per stage (2048 k)
 // bytes of one row per stage: 1152 (Q4_K), 1680 (Q6_K; a multiple of 16)
 __host__ __device__ constexpr int seg_bytes(int qt) { return kSegSB * (qt == kQ4 ? kQ4KBytes : kQ6KBytes); }
+// Shared-memory pitch of a stage row: seg_bytes for a TMA box; 32 more
+// bytes when the rows are staged one by one as 16-byte-aligned windows (a
+// matrix row pitch that is not a multiple of 16: Q6_K with K % 2048 != 0)
+__host__ __device__ constexpr bool row_copy_needed(int qt, int64_t K) { return qt != kQ4 && K % 2048 != 0; }
+__host__ __device__ constexpr int stage_row(int qt, int64_t K) {
+  return seg_bytes(qt) + (row_copy_needed(qt, K) ? 32 : 0);
+}
 constexpr int kSmemBudget = 200 * 1024;        // staged path (large nt*K)
 // Fused path: two CTAs (of consecutive kernels) share an SM, so each gets at
 // most half of the 228 KB less the 1 KB the hardware reserves per CTA; the
@@ -77,13 +84,13 @@ int64_t fused_act_bytes(int64_t nt, int64_t K) { return nt * fused_plane(K) + nt
 // fewer than kFusedMinStages fit next to the activations.
 int fused_stages(int qt, int64_t nt, int64_t K) {
   const int64_t fixed = ((fused_act_bytes(nt, K) + 15) & ~15) + 32 + 1024;
-  int64_t st = (kFusedCtaSmem - fixed) / (16 * seg_bytes(qt) + 16);
+  int64_t st = (kFusedCtaSmem - fixed) / (16 * stage_row(qt, K) + 16);
   if (st > kFusedMaxStages) st = kFusedMaxStages;
   return st >= kFusedMinStages ? (int)st : 0;
 }
 
 int stages_for(int qt, int64_t nt, int64_t K, int CR, int64_t budget) {
-  int s = (int)((budget - act_bytes_of(nt, K) - 1024 - 256) / ((int64_t)CR * seg_bytes(qt)));
+  int s = (int)((budget - act_bytes_of(nt, K) - 1024 - 256) / ((int64_t)CR * stage_row(qt, K)));
   return s > 8 ? 8 : s;
 }
 
@@ -106,10 +113,10 @@ __device__ __forceinline__ void named_arrive(int id, int threads) {
 
 template <int QT, int NT, int NW, int R, bool DOTS, bool FUSED>
 __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
-    mmvq_stream_kernel(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ x,
-                           int8_t* __restrict__ xq, float* __restrict__ xds, float* __restrict__ out,
-                           int32_t* __restrict__ dots, int od, int K, int stages, int* status, int static_w,
-                           int limit_ms, int skip_first) {
+    mmvq_stream_kernel(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restrict__ W,
+                           const float* __restrict__ x, int8_t* __restrict__ xq, float* __restrict__ xds,
+                           float* __restrict__ out, int32_t* __restrict__ dots, int od, int K, int stages,
+                           int* status, int static_w, int limit_ms, int skip_first) {
   using C = GemvCfg<QT, NW, R>;
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t s0 = smem_addr(smem_dyn);
@@ -121,7 +128,12 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
   const int Kp = FUSED ? ((K + 2047) & ~2047) : K;  // per-token stride of the code plane
   const int act_q = NT * Kp;                         // int8 codes
   const int act_bytes = act_q + NT * (K >> 5) * 8;
-  const int act_off = stages * C::STAGE_BYTES;
+  // rows staged by TMA boxes, or one by one (row_copy) when the matrix row
+  // pitch is not a multiple of 16 bytes
+  const bool row_copy = row_copy_needed(QT, K);
+  const int srow = stage_row(QT, K), stage_bytes = C::CR * srow;
+  const size_t row_bytes = (size_t)nsb * C::BLK;
+  const int act_off = stages * stage_bytes;
   const int bar_off = (act_off + act_bytes + 15) & ~15;
   const uint32_t full0 = sb + bar_off, empty0 = full0 + 8 * stages, act_bar = empty0 + 8 * stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + bar_off + 16 * stages + 8);
@@ -154,7 +166,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
   if (warp == NW) {
     // ----------------------------------------------------------- producer
     if (lane == 0 && nchunks > 0) {
-      prefetch_tmap(&tmW);
+      if (!row_copy) prefetch_tmap(&tmW);
       if (!static_w) griddep_wait();
       int issued = 0, st = 0, ph = 0, seg = 0, grp = g_begin;
       bool act_issued = FUSED;
@@ -170,8 +182,30 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         }
         if (!wait_bar(empty0 + 8 * st, ph ^ 1, g)) break;
         if (!(skip_first && c == 0)) {  // the stall test hook skips the first stage
-          mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE_BYTES);
-          tma_load_2d(sb + st * C::STAGE_BYTES, &tmW, seg * (C::SEG_BYTES / 8), grp * C::CR, full0 + 8 * st);
+          if (!row_copy) {
+            mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE_BYTES);
+            tma_load_2d(sb + st * C::STAGE_BYTES, &tmW, seg * (C::SEG_BYTES / 8), grp * C::CR, full0 + 8 * st);
+          } else {
+            // the stage's super-blocks of each of its rows, one window per row
+            const int nbs = min(kSegSB, nsb - seg * kSegSB);
+            const size_t total = (size_t)od * row_bytes;
+            uint32_t bytes = 0;
+            for (int r = 0; r < C::CR && grp * C::CR + r < od; ++r) {
+              const size_t start = (size_t)(grp * C::CR + r) * row_bytes + (size_t)seg * C::SEG_BYTES;
+              const RowWindow w = stage_row_window(start, start + (size_t)nbs * C::BLK, total,
+                                                   smem + st * stage_bytes + r * srow, W);
+              if (w.a1 > w.a0) bytes += (uint32_t)(w.a1 - w.a0);
+            }
+            mbar_arrive_expect_tx(full0 + 8 * st, bytes);
+            for (int r = 0; r < C::CR && grp * C::CR + r < od; ++r) {
+              const size_t start = (size_t)(grp * C::CR + r) * row_bytes + (size_t)seg * C::SEG_BYTES;
+              const size_t a0 = start & ~(size_t)15;
+              size_t a1 = (start + (size_t)nbs * C::BLK + 15) & ~(size_t)15;
+              if (a1 > (total & ~(size_t)15)) a1 = total & ~(size_t)15;
+              if (a1 > a0)
+                bulk_load(sb + st * stage_bytes + r * srow, W + a0, (uint32_t)(a1 - a0), full0 + 8 * st);
+            }
+          }
         }
         ++issued;
         if (++st == stages) {
@@ -291,7 +325,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
       if constexpr (QT == kQ4) {
       // the R weight rows of this lane: nibbles split into the low (sub-block
       // 2p) and high (sub-block 2p+1) planes, and the four scale factors
-      const uint8_t* stage = smem + st * C::STAGE_BYTES;
+      const uint8_t* stage = smem + st * stage_bytes;
       uint32_t lo[R][8], hi[R][8];
       float a_lo[R], a_hi[R], c_lo[R], c_hi[R];
 #pragma unroll
@@ -367,7 +401,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         }
       }
       } else {
-      const uint8_t* stage = smem + st * C::STAGE_BYTES;
+      const uint8_t* stage = smem + st * stage_bytes;
       // Q6_K: the lane's 64 values are quads 2(p%2), 2(p%2)+1 of half n = p/2:
       // low 4 bits from ql[64n + l] / ql[64n + 32 + l] (low nibbles for even p,
       // high for odd p), top 2 bits from qh[32n + l] (bits 0-1 / 2-3 for even p,
@@ -383,8 +417,10 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         uint32_t L0[8] = {}, L1[8] = {}, H[8] = {}, sw[1] = {0};
         uint32_t dbits = 0;
         if (use) {
-          const uint8_t* rowp = stage + (warp * R + i) * C::SEG_BYTES;  // 16-byte aligned
-          const int boff = sbo * kQ6KBytes;                              // even
+          const uint8_t* rowp = stage + (warp * R + i) * srow;  // 16-byte aligned
+          // even: the row's blocks start at its window's offset (0 for TMA boxes)
+          const int boff = (row_copy ? (int)(((size_t)(row0 + i) * row_bytes + (size_t)seg * C::SEG_BYTES) & 15) : 0) +
+                           sbo * kQ6KBytes;
           load_words_even<8>(rowp, boff + 64 * n, L0);
           load_words_even<8>(rowp, boff + 64 * n + 32, L1);
           load_words_even<8>(rowp, boff + 128 + 32 * n, H);
@@ -510,7 +546,7 @@ int launch_stream(const GemvArgs& a, int stages) {
   if (cudaGetDevice(&dev) != cudaSuccess) return QMM_EDEVICE;
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   const int64_t act_bytes = FUSED ? fused_act_bytes(NT, a.K) : act_bytes_of(NT, a.K);
-  const int smem = stages * C::STAGE_BYTES + (int)((act_bytes + 15) & ~15) + 16 * stages + 32 + 1024;
+  const int smem = stages * C::CR * stage_row(QT, a.K) + (int)((act_bytes + 15) & ~15) + 16 * stages + 32 + 1024;
   auto kern = mmvq_stream_kernel<QT, NT, NW, R, DOTS, FUSED>;
   static PerDevice<bool> attr_done;
   if (int rc = smem_attr_once(kern, kSmemBudget + 8192, attr_done, dev)) return rc;
@@ -519,12 +555,15 @@ int launch_stream(const GemvArgs& a, int stages) {
   if (!fn) return QMM_ELAUNCH;
   // W viewed as [od][row_bytes/8] 8-byte elements; one box = CR rows x 8 super-blocks
   const uint64_t row_bytes = (uint64_t)(a.K / 256) * C::BLK;
-  CUtensorMap m;
+  CUtensorMap m = {};
   const cuuint64_t dims[2] = {row_bytes / 8, (cuuint64_t)a.od};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {C::SEG_BYTES / 8, (cuuint32_t)C::CR};
   const cuuint32_t estr[2] = {1, 1};
-  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(a.W), dims, strides, box, estr,
+  // rows whose pitch is not a multiple of 16 bytes are staged by the kernel
+  // itself, one window per row
+  if (!row_copy_needed(QT, a.K) &&
+      fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(a.W), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return QMM_ELAUNCH;
@@ -533,7 +572,8 @@ int launch_stream(const GemvArgs& a, int stages) {
   if (grid > groups) grid = groups;
   const int iod = (int)a.od, iK = (int)a.K, sw = a.static_w ? 1 : 0;
   const int stall = stall_ms();
-  return launch_ex(kern, dim3(grid), dim3(C::THREADS), (size_t)smem, a.stream, a.pdl, m, a.x, a.xq, a.xds,
+  return launch_ex(kern, dim3(grid), dim3(C::THREADS), (size_t)smem, a.stream, a.pdl, m,
+                   static_cast<const uint8_t*>(a.W), a.x, a.xq, a.xds,
                    a.out, a.dots, iod, iK, stages, a.status, sw, stall > 0 ? stall : 4000, stall > 0 ? 1 : 0);
 }
 
@@ -596,10 +636,11 @@ int launch_fused_nt(const GemvArgs& a, int64_t nt) {
 
 int qt_of(int qtype) { return qtype == QMM_Q4_K ? kQ4 : kQ6; }
 
-// Q6_K rows are whole 16-byte multiples (a TMA row pitch) only when K is a
-// multiple of 2048 (8 blocks of 210 bytes = 1680).
+// Both types at any K % 256 (Q6_K rows with a pitch that is not a multiple of
+// 16 bytes are staged row by row).
 bool gemv_type_ok(int qtype, int64_t K) {
-  return qtype == QMM_Q4_K || (qtype == QMM_Q6_K && K % 2048 == 0);
+  (void)K;
+  return qtype == QMM_Q4_K || qtype == QMM_Q6_K;
 }
 
 }  // namespace

@@ -71,6 +71,15 @@ struct MC {
   static constexpr int STAGE = kTileRows * PITCH;
 };
 
+// Rows whose pitch is not a multiple of 16 bytes (Q6_K with K % 2048 != 0)
+// cannot be described by a TMA tensor map: the producer stages them one by
+// one as 16-byte-aligned windows, in rows 32 bytes wider (1712 = 48 mod 128,
+// still conflict-free for the 4-byte reads of rows g = 0..3).
+__host__ __device__ constexpr bool mma_row_copy(int qt, int64_t K) { return qt != kQ4 && K % 2048 != 0; }
+__host__ __device__ constexpr int mma_pitch(int qt, int64_t K) {
+  return qt == kQ4 ? MC<kQ4>::PITCH : MC<kQ6>::PITCH + (mma_row_copy(qt, K) ? 32 : 0);
+}
+
 // Shared-memory plan of one launch (host and device agree on it).  The raw
 // (d, s) pairs of the activations are staged in the coefficient and
 // tile-sum areas, which are free until the main loop starts.
@@ -83,7 +92,7 @@ struct Plan {
 
 __host__ __device__ inline Plan make_plan(int qt, int ntl, int nt, int K, int stages, int x16) {
   Plan p;
-  const int stage_bytes = kTileRows * (qt == kQ4 ? MC<kQ4>::PITCH : MC<kQ6>::PITCH);
+  const int stage_bytes = kTileRows * mma_pitch(qt, K);
   p.stages = stages;
   p.x16 = x16;
   // x16: 64 bytes per (token, block), pitch = 64 (mod 128), the raw codes
@@ -143,6 +152,11 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
   const int nsb = K >> 8, nbk = K >> 5, nseg = (nsb + kSegSB - 1) / kSegSB;
   const int np = 4 * NTL;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // stage row pitch, and the matrix row pitch for the per-row window offsets
+  // of rows staged one by one (0 offset for TMA boxes)
+  const bool row_copy = mma_row_copy(QT, K);
+  const int pitch = mma_pitch(QT, K), stage_sz = kTileRows * pitch;
+  const size_t row_bytes = (size_t)nsb * C::BLK;
   const uint32_t rfree0 = red0 + 16;  // red0: two "partials written" barriers, then two "sums read"
   uint8_t* xw = smem + P.x_off;
   bool ok = __all_sync(0xffffffffu, wait_bar(xbar, 0, gd));
@@ -274,8 +288,12 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
   for (int it = 0; it < nitems && ok; ++it) {
     ok = __all_sync(0xffffffffu, wait_bar(full0 + 8 * st, ph, gd));
     if (!ok) break;
-    const uint8_t* stage = smem + st * C::STAGE;
+    const uint8_t* stage = smem + st * stage_sz;
     const int r0 = tile * kTileRows;
+    // offset of the stage's first block in row r's window (row copies only)
+    auto row_shift = [&](int r) -> int {
+      return row_copy ? (int)(((size_t)(r0 + r) * row_bytes + (size_t)seg * C::SEG) & 15) : 0;
+    };
     if constexpr (QT == kQ4) {
       // warp -> super-block warp/2 of the stage, block pairs 2(warp&1) and 2(warp&1)+1
       const int sbl = warp >> 1, ps = warp & 1, sbi = seg * kSegSB + sbl;
@@ -336,10 +354,12 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
       // Q6_K: warp -> super-blocks 2k and 2k+1 (k = warp/4), half h, quads
       // 2qp and 2qp+1 of that half: four blocks, two of each alignment
       const int k2 = 2 * (warp >> 2), h = (warp >> 1) & 1, qp = warp & 1;
+      // (super-blocks past the row's end, in a partial last stage, are skipped:
+      // rows staged one by one carry the next row's bytes there, not zeros)
       {  // coefficients, 16 rows x 4 blocks x 2 groups: lane -> row lane/2, super-block 2k + (lane&1)
         const int row = lane >> 1, u = lane & 1;
-        const uint8_t* rowp = stage + row * C::PITCH;
-        const int boff = (k2 + u) * kQ6KBytes;
+        const uint8_t* rowp = stage + row * pitch;
+        const int boff = row_shift(row) + (k2 + u) * kQ6KBytes;
         const uint32_t sw = word_even(rowp, boff + 192 + 8 * h + 4 * qp);  // scales of groups 8h+4qp..+3
         const float d = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rowp + boff + 208)) * 0x1p24f;
         float v[4];
@@ -353,20 +373,21 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int sbl = k2 + u, sbi = seg * kSegSB + sbl;
-        const uint8_t* rg = stage + g * C::PITCH;
-        const uint8_t* rh = rg + 8 * C::PITCH;
-        const int boff = sbl * kQ6KBytes;
+        if (sbi >= nsb) break;
+        const uint8_t* rg = stage + g * pitch;
+        const uint8_t* rh = rg + 8 * pitch;
+        const int boff = sbl * kQ6KBytes, sg = row_shift(g), sh = row_shift(g + 8);
         // words of rows g and g+8 for steps s = 0, 1: ql of quads 2qp, 2qp+1; qh
         uint32_t QL[2][2][2], QH[2][2];
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           const int o = boff + 64 * h + 16 * s + 4 * c, oh = boff + 128 + 32 * h + 16 * s + 4 * c;
-          QL[0][s][0] = word_even(rg, o);
-          QL[0][s][1] = word_even(rg, o + 32);
-          QH[0][s] = word_even(rg, oh);
-          QL[1][s][0] = word_even(rh, o);
-          QL[1][s][1] = word_even(rh, o + 32);
-          QH[1][s] = word_even(rh, oh);
+          QL[0][s][0] = word_even(rg, sg + o);
+          QL[0][s][1] = word_even(rg, sg + o + 32);
+          QH[0][s] = word_even(rg, sg + oh);
+          QL[1][s][0] = word_even(rh, sh + o);
+          QL[1][s][1] = word_even(rh, sh + o + 32);
+          QH[1][s] = word_even(rh, sh + oh);
         }
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
@@ -463,7 +484,8 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
 
 template <int QT, int NTL, bool X16, bool DOTS>
 __global__ void __launch_bounds__(kThreads, 1)
-    mmvq_mma_kernel(const __grid_constant__ CUtensorMap tmW, const int8_t* __restrict__ xq, const float* __restrict__ xds,
+    mmvq_mma_kernel(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restrict__ W,
+                    const int8_t* __restrict__ xq, const float* __restrict__ xds,
                     float* __restrict__ out, int32_t* __restrict__ dots, int od, int K, int nt, int stages,
                     int* status, int static_w, int limit_ms, int skip_first) {
   using C = MC<QT>;
@@ -502,15 +524,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kNW) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
-      prefetch_tmap(&tmW);
+      const bool row_copy = mma_row_copy(QT, K);
+      const int pitch = mma_pitch(QT, K), stage_sz = kTileRows * pitch;
+      const size_t row_bytes = (size_t)nsb * C::BLK, total = (size_t)od * row_bytes;
+      if (!row_copy) prefetch_tmap(&tmW);
       int issued = 0, st = 0, ph = 0, seg = 0, tile = t_begin;
       // one box: 16 rows x PITCH bytes from super-block 8*seg (rows past od
       // and bytes past the row's end arrive zero-filled)
       auto issue = [&]() -> bool {
         if (!wait_bar(empty0 + 8 * st, ph ^ 1, gd)) return false;
         if (!(skip_first && issued == 0)) {  // the stall test hook skips the first stage
-          mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE);
-          tma_load_2d(sb + st * C::STAGE, &tmW, seg * (C::SEG / 8), tile * kTileRows, full0 + 8 * st);
+          if (!row_copy) {
+            mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE);
+            tma_load_2d(sb + st * C::STAGE, &tmW, seg * (C::SEG / 8), tile * kTileRows, full0 + 8 * st);
+          } else {
+            // the stage's super-blocks of each of its rows, one window per row
+            const int nbs = min(kSegSB, nsb - seg * kSegSB);
+            uint32_t bytes = 0;
+            for (int r = 0; r < kTileRows && tile * kTileRows + r < od; ++r) {
+              const size_t start = (size_t)(tile * kTileRows + r) * row_bytes + (size_t)seg * C::SEG;
+              const RowWindow w = stage_row_window(start, start + (size_t)nbs * C::BLK, total,
+                                                   smem + st * stage_sz + r * pitch, W);
+              if (w.a1 > w.a0) bytes += (uint32_t)(w.a1 - w.a0);
+            }
+            mbar_arrive_expect_tx(full0 + 8 * st, bytes);
+            for (int r = 0; r < kTileRows && tile * kTileRows + r < od; ++r) {
+              const size_t start = (size_t)(tile * kTileRows + r) * row_bytes + (size_t)seg * C::SEG;
+              const size_t a0 = start & ~(size_t)15;
+              size_t a1 = (start + (size_t)nbs * C::BLK + 15) & ~(size_t)15;
+              if (a1 > (total & ~(size_t)15)) a1 = total & ~(size_t)15;
+              if (a1 > a0) bulk_load(sb + st * stage_sz + r * pitch, W + a0, (uint32_t)(a1 - a0), full0 + 8 * st);
+            }
+          }
         }
         ++issued;
         if (++st == stages) {
@@ -585,12 +630,15 @@ int launch_mma_cfg(const void* W, const int8_t* xq, const float* xds, float* out
   auto fn = tensor_map_encoder();
   if (!fn) return QMM_ELAUNCH;
   const uint64_t row_bytes = (uint64_t)(K / 256) * C::BLK;
-  CUtensorMap m;
+  CUtensorMap m = {};
   const cuuint64_t dims[2] = {row_bytes / 8, (cuuint64_t)od};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {(cuuint32_t)(C::PITCH / 8), (cuuint32_t)kTileRows};
   const cuuint32_t estr[2] = {1, 1};
-  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(W), dims, strides, box, estr,
+  // rows whose pitch is not a multiple of 16 bytes are staged by the kernel
+  // itself, one window per row
+  if (!mma_row_copy(QT, K) &&
+      fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(W), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return QMM_ELAUNCH;
@@ -598,7 +646,8 @@ int launch_mma_cfg(const void* W, const int8_t* xq, const float* xds, float* out
   const int stall = stall_ms();
   int grid = nsm > 0 ? nsm : 152;
   if (grid > tiles) grid = (int)tiles;
-  return launch_ex(kern, dim3(grid), dim3(kThreads), (size_t)p.total + 1024, stream, pdl, m, xq, xds, out, dots,
+  return launch_ex(kern, dim3(grid), dim3(kThreads), (size_t)p.total + 1024, stream, pdl, m,
+                   static_cast<const uint8_t*>(W), xq, xds, out, dots,
                    (int)od, (int)K, (int)nt, p.stages, status, static_w ? 1 : 0, stall > 0 ? stall : 4000,
                    stall > 0 ? 1 : 0);
 }
@@ -623,7 +672,6 @@ int launch_mma_qt(const void* W, const int8_t* xq, const float* xds, float* out,
 
 bool mmvq_mma_fits(int qtype, int64_t nt, int64_t K) {
   if (qtype != QMM_Q4_K && qtype != QMM_Q6_K) return false;
-  if (qtype == QMM_Q6_K && K % 2048) return false;
   if (nt < 1 || nt > kMmaMaxNt) return false;
   Plan p;
   return choose_plan(qtype == QMM_Q4_K ? kQ4 : kQ6, nt <= 8 ? 1 : 2, nt, K, &p);

@@ -49,7 +49,7 @@ def test_argument_checks_need_no_device():
     assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 300, 1, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 256, 17, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 0, 256, 1, 0) == qmm.QMM_EINVAL_SHAPE
-    assert qmm.qmm_gemv(qmm.Q6_K, p, p, p, p, 256, 1024, 1, 0) == qmm.QMM_EINVAL_SHAPE  # Q6_K: K % 2048
+    assert qmm.qmm_gemv(qmm.Q6_K, p, p, p, p, 256, 1000, 1, 0) == qmm.QMM_EINVAL_SHAPE  # K % 256
     assert qmm.qmm_gemv(qmm.Q4_K, p + 1, p, p, p, 256, 256, 1, 0) == qmm.QMM_EALIGN
     assert qmm.qmm_quantize_q8_1(p, 1, 48, p, p, 0) == qmm.QMM_EINVAL_SHAPE
     assert qmm.qmm_gemm(qmm.Q4_K, p, p, p, p, 256, 256, 0, p, 4096, 0) == qmm.QMM_EINVAL_SHAPE
@@ -78,8 +78,7 @@ def test_matmul_route_query():
     while the activations leave room for its weight ring, quantize + the
     warp-MMA MMVQ from 5 tokens (Q4_K) or 2 (Q6_K) up to 16 where it fits,
     quantize + the dp4a MMVQ for the other nt <= 8, the tensor-core GEMM
-    beyond and for Q6_K rows the MMVQ kernels cannot stage (K % 2048 != 0);
-    workspace is needed exactly on the GEMM route."""
+    beyond; workspace is needed exactly on the GEMM route."""
     Q4, Q6 = qmm.Q4_K, qmm.Q6_K
     F, V, G = qmm.QMM_PATH_FUSED_MMVQ, qmm.QMM_PATH_MMVQ, qmm.QMM_PATH_MMQ
     cases = [((Q4, 4096, 4096, 1), F), ((Q4, 11008, 4096, 1), F), ((Q4, 256, 512, 4), F),
@@ -90,9 +89,9 @@ def test_matmul_route_query():
              ((Q6, 32000, 4096, 2), V), ((Q6, 4096, 4096, 8), V), ((Q6, 4096, 4096, 9), V),
              ((Q6, 4096, 4096, 17), G), ((Q6, 32000, 4096, 80), G),
              # Q6_K rows whose pitch is not a multiple of 16 bytes (K % 2048 != 0)
-             # are staged row by row: only the tensor-core route takes them
-             ((Q6, 4096, 768, 32), G), ((Q6, 4096, 11008, 1), G), ((Q6, 4096, 2304, 8), G),
-             ((Q6, 300, 256, 64), G)]
+             # are staged row by row, on every route
+             ((Q6, 4096, 768, 32), G), ((Q6, 4096, 11008, 1), F), ((Q6, 4096, 2304, 8), V),
+             ((Q6, 300, 256, 64), G), ((Q6, 4096, 11008, 2), V)]
     for args, path in cases:
         assert qmm.qmm_matmul_path(*args) == path, args
         assert (qmm.qmm_matmul_workspace_bytes(*args) > 0) == (path == qmm.QMM_PATH_MMQ), args

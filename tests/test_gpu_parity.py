@@ -415,9 +415,8 @@ def test_errors_and_bounded_wait():
                         ws.data_ptr(), 64, st) == qmm.QMM_EINVAL_QTYPE
     assert qmm.qmm_gemv(Q4_K, Wd.data_ptr() + 8, xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 8,
                         st) == qmm.QMM_EALIGN
-    # the MMVQ kernels stage Q6_K rows by TMA, which needs a 16-byte row pitch
-    # (K % 2048 == 0); other K take the tensor-core route
-    assert qmm.qmm_gemv(Q6_K, Wd.data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 16,
+    # a shape the MMVQ kernels refuse
+    assert qmm.qmm_gemv(Q6_K, Wd.data_ptr(), xq.data_ptr(), xds.data_ptr(), out.data_ptr(), 256, 512, 17,
                         st) == qmm.QMM_EINVAL_SHAPE
     # bounded wait: a skipped producer arrival makes the waits give up and report
     assert qmm.qmm_sync_status(st) == qmm.QMM_OK
@@ -467,16 +466,19 @@ def test_mmvq_bounded_wait(route, nt):
     assert_close_rows(got, ref, f"{route} nt={nt} after timeout")
 
 
-@pytest.mark.parametrize("od,K,nt", [(300, 11008, 1), (300, 11008, 8), (300, 11008, 64), (257, 2304, 1),
-                                     (257, 2304, 8), (257, 2304, 64), (129, 256, 70), (64, 768, 130)])
+@pytest.mark.parametrize("od,K,nt", [(300, 11008, 1), (300, 11008, 2), (300, 11008, 8), (300, 11008, 64),
+                                     (257, 2304, 1), (257, 2304, 8), (257, 2304, 64), (129, 256, 70),
+                                     (64, 768, 130), (33, 768, 5), (4096, 11008, 1)])
 def test_q6k_any_k(od, K, nt):
     """Q6_K rows whose pitch (210*K/256 bytes) is not a multiple of 16 -- K %
     2048 != 0, e.g. K = 11008, a Llama-7B FFN-down width -- cannot be a TMA
-    tensor map; the tensor-core GEMM stages them row by row (16-byte-aligned
-    windows, the last row's tail by ordinary loads) for every nt.  Outputs
-    within tolerance, q8_1 bit-exact, the exact folded block sums, and a
-    deterministic repeat."""
-    assert qmm.qmm_matmul_path(Q6_K, od, K, nt) == qmm.QMM_PATH_MMQ
+    tensor map; every route stages them row by row (16-byte-aligned windows,
+    the last row's tail by ordinary loads): the fused dp4a MMVQ at nt = 1, the
+    warp-MMA MMVQ for a few tokens, the tensor-core GEMM beyond.  Outputs
+    within tolerance, q8_1 bit-exact, the exact block sums of the route's dot
+    code, and a deterministic repeat."""
+    route = qmm.qmm_matmul_path(Q6_K, od, K, nt)
+    assert route == (qmm.QMM_PATH_MMQ if nt > 16 else qmm.QMM_PATH_FUSED_MMVQ if nt == 1 else qmm.QMM_PATH_MMVQ)
     W, x = _case(Q6_K, od, K, nt, outliers=True, seed=K + nt)
     Wd, xd = dev(W, torch), dev(x, torch)
     out, xq, xds = qmm.matmul(Q6_K, Wd, xd, od, return_q8=True)
@@ -487,7 +489,12 @@ def test_q6k_any_k(od, K, nt):
     assert_close_rows(got, ref, f"q6k {od}x{K} nt={nt}")
     again = qmm.matmul(Q6_K, Wd, xd, od).cpu().numpy()
     assert np.array_equal(again.view(np.uint32), got.view(np.uint32))
-    d = qmm.block_dots(Q6_K, Wd, dev(oq, torch), dev(ods, torch), od, path=1)
+    if route == qmm.QMM_PATH_MMQ:
+        d = qmm.block_dots(Q6_K, Wd, dev(oq, torch), dev(ods, torch), od, path=1)
+        want = _tc_dots_expected(Q6_K, W, oq, od)
+    else:
+        d = qmm.block_dots(Q6_K, Wd, dev(oq, torch), dev(ods, torch), od, path=0 if nt == 1 else 2)
+        want = ora().block_dots(Q6_K, W, oq, od)
     torch.cuda.synchronize()
     assert qmm.qmm_sync_status(0) == qmm.QMM_OK
-    assert np.array_equal(d.cpu().numpy().astype(np.int64), _tc_dots_expected(Q6_K, W, oq, od))
+    assert np.array_equal(d.cpu().numpy().astype(np.int64), want.astype(np.int64))
