@@ -430,8 +430,8 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 // spill one of them in between, which reads it before the data has arrived
 // (wrong values in a few columns of one warp's load, more often under
 // register pressure).  Here the outputs exist only after the wait.
-// 64 columns (two 32-column loads at taddr and taddr + 32) with one wait.
-__device__ __forceinline__ void tc_ld_32x32_x2_sync(uint32_t taddr, uint32_t (&v)[64]) {
+// Two 32-column loads (at taddr0 and taddr1) with one wait.
+__device__ __forceinline__ void tc_ld_32x32_x2_sync(uint32_t taddr0, uint32_t taddr1, uint32_t (&v)[64]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
@@ -446,7 +446,7 @@ __device__ __forceinline__ void tc_ld_32x32_x2_sync(uint32_t taddr, uint32_t (&v
         "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]),
         "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
         "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
-      : "r"(taddr), "r"(taddr + 32u)
+      : "r"(taddr0), "r"(taddr1)
       : "memory");
 }
 

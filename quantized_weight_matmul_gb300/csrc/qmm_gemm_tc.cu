@@ -104,6 +104,10 @@ struct Cfg {
   // (a Q6_K block, with its hi and lo operands, is twice a Q4_K block's).
   static constexpr int ACOLS = QT == kQ4 ? 32 : 64;
   static constexpr int NBUF = (512 - AS * ACOLS) / BN;
+  // Q6_K with the 64-token tile: the two 32-value blocks of a stage share one
+  // accumulator pair, one commit and one release (NBUF / 2 pairs), so each
+  // MMA -> epilogue -> MMA round trip carries a whole stage
+  static constexpr bool PAIRED = QT == kQ6 && BN == 64;
   static constexpr int A_COL0 = NBUF * BN;
   static_assert(NBUF >= 2 && NBUF <= 8, "accumulator ring");
   static_assert(A_COL0 % 16 == 0 && ACOLS % 16 == 0, "TMEM column alignment");
@@ -486,6 +490,27 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
             tc_commit(bars.raw_empty(rs));  // the raw stage's min operands were read
             advance();
           }
+          if constexpr (C::PAIRED) {
+            // both blocks into one accumulator pair, one commit: the ring's
+            // slots are pairs here (slot < NBUF / 2, BN columns apart)
+            if (!gwait(bars.acc_empty(slot), ph ^ 1u, g)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t dp = tmem + slot * (uint32_t)(2 * BN);
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                tc_mma_f16_tmem_a(dp + (uint32_t)(gi * BN), a_t + 32 * gi + 8 * i,
+                                  bd + (uint64_t)(2 * (2 * gi + (i >> 1))), idesc, i > 0 ? 1u : 0u);
+            tc_commit(bars.acc_full(slot));
+            if (++slot == (uint32_t)(C::NBUF / 2)) {
+              slot = 0;
+              ph ^= 1u;
+            }
+          } else
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi) {
             if (!acquire(d_t)) {
@@ -671,7 +696,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
         // both 32-column chunks with one wait, then the accumulator goes back
         uint32_t P2[64];
         __syncwarp();
-        tc_ld_32x32_x2_sync(t_acc, P2);
+        tc_ld_32x32_x2_sync(t_acc, t_acc + 32, P2);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty);
@@ -726,6 +751,50 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
           if (!ok) break;
         }
         const float* scp = reinterpret_cast<const float*>(smem + C::SC_OFF + bs * C::SC_BYTES);
+        if constexpr (C::PAIRED) {
+          // the stage's two blocks: one wait, both loads, one release
+          if (!warp_wait(bars.acc_full(slot), ph, g)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t t_acc = tmem + lane_base + slot * (uint32_t)(2 * BN) + (uint32_t)(cb * CPW);
+          const uint32_t bar_empty = bars.acc_empty(slot);
+          if (++slot == (uint32_t)(C::NBUF / 2)) {
+            slot = 0;
+            ph ^= 1u;
+          }
+          uint32_t P2[64];
+          __syncwarp();
+          tc_ld_32x32_x2_sync(t_acc, t_acc + BN, P2);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_empty);
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            const uint32_t* P = P2 + 32 * gi;
+            if constexpr (DOTS) {
+              const int grp = 8 * (b + b_off) + 2 * s + gi;
+              const size_t ng = (size_t)(K >> 5), tstride = (size_t)od * ng;
+              const int t0 = tok0 + cb * CPW;
+              int32_t* dpp = dots + ((size_t)t0 * od + row_g) * ng + grp;
+              const int nv = row_ok ? min(32, nt - t0) : 0;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nv) dpp[i * tstride] = __float2int_rn(__uint_as_float(P[i]));
+            } else {
+              const float* dxp = scp + gi * BN + cb * CPW;
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(dxp + i);
+                acc[i] = fmaf(v.x, __uint_as_float(P[i]), acc[i]);
+                acc[i + 1] = fmaf(v.y, __uint_as_float(P[i + 1]), acc[i + 1]);
+                acc[i + 2] = fmaf(v.z, __uint_as_float(P[i + 2]), acc[i + 2]);
+                acc[i + 3] = fmaf(v.w, __uint_as_float(P[i + 3]), acc[i + 3]);
+              }
+            }
+          }
+        } else
 #pragma unroll
         for (int gi = 0; gi < 2 && ok; ++gi) {
           const float* dxp = scp + gi * BN + cb * CPW;  // dx of this block's tokens
