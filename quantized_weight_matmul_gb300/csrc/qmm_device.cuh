@@ -247,33 +247,58 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // value.  With r = fl(1/d), y = fl(x*r) is within |x/d| * 2^-23 < 1.6e-5 of
 // x/d (|x/d| <= 127.00001), and fl(x/d) within 2^-24 * |x/d| < 7.6e-6 of it,
 // so when y is more than 1e-4 away from every half-integer, y and fl(x/d) lie
-// inside the same rounding interval and rint(y) is the code.  A value that
-// close to a half-integer (or every value, when 1/d overflows) takes the
-// correctly rounded division instead; the warp votes first so that the
-// divisions run only when some lane needs one.  All 32 lanes of the warp must
-// call this together.
+// inside the same rounding interval and rint(y) is the code.  rint(y) is taken
+// by adding 1.5 * 2^23: the sum lies in [2^23, 2^24), where the f32 spacing
+// is 1, so the addition rounds y to an integer, ties to even, and the low bits
+// of the sum hold that integer in two's complement.  |y| < 127.5 here, so no
+// clamp is needed.  A value that close to a half-integer (or every value, when
+// 1/d overflows) takes the correctly rounded division instead; the warp votes
+// first so that the divisions run only when some lane needs one.  All 32
+// lanes of the warp must call this together.
+//
+// Output: c[i] is a word whose low byte is code i (two's complement).
 template <int N>
-__device__ __forceinline__ void q8_codes(const float (&v)[N], float d, int (&q)[N]) {
+__device__ __forceinline__ void q8_code_words(const float (&v)[N], float d, uint32_t (&c)[N]) {
   static_assert(N <= 32, "one bit per value");
+  constexpr float kRound = 0x1.8p23f;  // 1.5 * 2^23
   uint32_t near = 0;
 #pragma unroll
-  for (int i = 0; i < N; ++i) q[i] = 0;
+  for (int i = 0; i < N; ++i) c[i] = 0;
   if (d != 0.0f) {
     const float r = __frcp_rn(d);
     if (!(r < INFINITY)) near = N == 32 ? 0xFFFFFFFFu : (1u << N) - 1u;
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-      const float y = v[i] * r;
-      const float n = rintf(y);
+      const float y = __fmul_rn(v[i], r);
+      const float t = __fadd_rn(y, kRound);
+      const float n = __fsub_rn(t, kRound);
       if (fabsf(fabsf(y - n) - 0.5f) <= 1e-4f) near |= 1u << i;
-      q[i] = max(-127, min(127, (int)n));
+      c[i] = __float_as_uint(t);
     }
   }
   if (__any_sync(0xffffffffu, near != 0)) {
 #pragma unroll
     for (int i = 0; i < N; ++i)
-      if (near & (1u << i)) q[i] = max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], d))));
+      if (near & (1u << i)) c[i] = (uint32_t)max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], d))));
   }
+}
+
+// The same codes as signed integers.
+template <int N>
+__device__ __forceinline__ void q8_codes(const float (&v)[N], float d, int (&q)[N]) {
+  uint32_t c[N];
+  q8_code_words<N>(v, d, c);
+#pragma unroll
+  for (int i = 0; i < N; ++i) q[i] = (int)(int8_t)(c[i] & 0xFFu);
+}
+
+// The low bytes of four words, packed in order into one word.
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  uint32_t ab, cd, r;
+  asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(ab) : "r"(a), "r"(b));
+  asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(cd) : "r"(c), "r"(d));
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(r) : "r"(ab), "r"(cd));
+  return r;
 }
 
 // Dot product of the four unsigned bytes of a with the four signed bytes of b,

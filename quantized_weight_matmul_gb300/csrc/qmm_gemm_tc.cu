@@ -659,9 +659,11 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
     const size_t row_bytes = (size_t)nsb_all * (QT == kQ4 ? kQ4KBytes : kQ6KBytes);
     const uint8_t* wrow = W + (size_t)row_c * row_bytes;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    float acc[CPW];
+    // the running sums as packed f32 pairs (columns 2i, 2i+1): one FMA-pipe
+    // instruction per two outputs
+    f2 acc[CPW / 2];
 #pragma unroll
-    for (int i = 0; i < CPW; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < CPW / 2; ++i) acc[i] = pk2(0.0f, 0.0f);
     float sigma = 1.0f;  // acc holds (partial sum) / sigma
     uint32_t slot = 0, ph = 0;
     int bs = 0;
@@ -680,9 +682,31 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
       else
         h_next = __ldg(reinterpret_cast<const uint16_t*>(wrow + (size_t)(bb + b_off) * kQ6KBytes + 208));
     };
+    // acc[16c .. 16c+15] += dx[32c .. 32c+31] * P: the chunk's 32 dx values
+    // are all loaded first (broadcast shared-memory loads), so their latency
+    // is paid once per chunk
+    auto fma_chunk = [&](int c, const float* dxp, const uint32_t(&P)[32]) {
+      float4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = *reinterpret_cast<const float4*>(dxp + 32 * c + 4 * q);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        f2& a0 = acc[16 * c + 2 * q];
+        f2& a1 = acc[16 * c + 2 * q + 1];
+        a0 = fma2(pk2(v[q].x, v[q].y), pk2(__uint_as_float(P[4 * q]), __uint_as_float(P[4 * q + 1])), a0);
+        a1 = fma2(pk2(v[q].z, v[q].w), pk2(__uint_as_float(P[4 * q + 2]), __uint_as_float(P[4 * q + 3])), a1);
+      }
+    };
+    // acc[16c ..] += m * P (the min-term entry; m is the same for every column)
+    auto fma_chunk_scalar = [&](int c, float m, const uint32_t(&P)[32]) {
+      const f2 m2 = pk2(m, m);
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        acc[16 * c + q] = fma2(m2, pk2(__uint_as_float(P[2 * q]), __uint_as_float(P[2 * q + 1])), acc[16 * c + q]);
+    };
     // one accumulator entry: wait, read this warp's CPW columns 32 at a time,
-    // hand the accumulator back right after the last read (the values are in
-    // registers), apply f(chunk, P) to each chunk
+    // hand the accumulator back right after the last read, apply f(chunk, P)
+    // to each chunk as soon as it is in registers
     auto entry = [&](auto&& f) -> bool {
       if (!warp_wait(bars.acc_full(slot), ph, g)) return false;
       tc_fence_after();
@@ -692,29 +716,17 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
         slot = 0;
         ph ^= 1u;
       }
-      if constexpr (CH == 2) {
-        // both 32-column chunks with one wait, then the accumulator goes back
-        uint32_t P2[64];
-        __syncwarp();
-        tc_ld_32x32_x2_sync(t_acc, t_acc + 32, P2);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty);
-        f(0, *reinterpret_cast<const uint32_t(*)[32]>(&P2[0]));
-        f(1, *reinterpret_cast<const uint32_t(*)[32]>(&P2[32]));
-      } else {
 #pragma unroll
-        for (int c = 0; c < CH; ++c) {
-          uint32_t P[32];
+      for (int c = 0; c < CH; ++c) {
+        uint32_t P[32];
+        __syncwarp();
+        tc_ld_32x32_sync(t_acc + 32 * c, P);
+        if (c == CH - 1) {
+          tc_fence_before();
           __syncwarp();
-          tc_ld_32x32_sync(t_acc + 32 * c, P);
-          if (c == CH - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty);
-          }
-          f(c, P);
+          if (lane == 0) mbar_arrive(bar_empty);
         }
+        f(c, P);
       }
       return true;
     };
@@ -731,8 +743,9 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
           const float ratio = sigma * __fdividef(1.0f, d);
           sigma = d;
           if (b > 0) {
+            const f2 r2 = pk2(ratio, ratio);
 #pragma unroll
-            for (int i = 0; i < CPW; ++i) acc[i] *= ratio;
+            for (int i = 0; i < CPW / 2; ++i) acc[i] = mul2(acc[i], r2);
           }
         }
         if (QT == kQ4) mc = -half_bits_to_float(h >> 16) * __fdividef(1.0f, sigma);
@@ -744,10 +757,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
           break;
         }
         if (MIN && s == 0) {
-          ok = entry([&](int c, const uint32_t(&P)[32]) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(mc, __uint_as_float(P[i]), acc[32 * c + i]);
-          });
+          ok = entry([&](int c, const uint32_t(&P)[32]) { fma_chunk_scalar(c, mc, P); });
           if (!ok) break;
         }
         const float* scp = reinterpret_cast<const float*>(smem + C::SC_OFF + bs * C::SC_BYTES);
@@ -764,15 +774,16 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
             slot = 0;
             ph ^= 1u;
           }
-          uint32_t P2[64];
-          __syncwarp();
-          tc_ld_32x32_x2_sync(t_acc, t_acc + BN, P2);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_empty);
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi) {
-            const uint32_t* P = P2 + 32 * gi;
+            uint32_t P[32];
+            __syncwarp();
+            tc_ld_32x32_sync(t_acc + (uint32_t)(gi * BN), P);
+            if (gi == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_empty);
+            }
             if constexpr (DOTS) {
               const int grp = 8 * (b + b_off) + 2 * s + gi;
               const size_t ng = (size_t)(K >> 5), tstride = (size_t)od * ng;
@@ -783,15 +794,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
               for (int i = 0; i < 32; ++i)
                 if (i < nv) dpp[i * tstride] = __float2int_rn(__uint_as_float(P[i]));
             } else {
-              const float* dxp = scp + gi * BN + cb * CPW;
-#pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                const float4 v = *reinterpret_cast<const float4*>(dxp + i);
-                acc[i] = fmaf(v.x, __uint_as_float(P[i]), acc[i]);
-                acc[i + 1] = fmaf(v.y, __uint_as_float(P[i + 1]), acc[i + 1]);
-                acc[i + 2] = fmaf(v.z, __uint_as_float(P[i + 2]), acc[i + 2]);
-                acc[i + 3] = fmaf(v.w, __uint_as_float(P[i + 3]), acc[i + 3]);
-              }
+              fma_chunk(0, scp + gi * BN + cb * CPW, P);
             }
           }
         } else
@@ -809,15 +812,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
               for (int i = 0; i < 32; ++i)
                 if (i < nv) dp[i * tstride] = __float2int_rn(__uint_as_float(P[i]));
             } else {
-#pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                const float4 v = *reinterpret_cast<const float4*>(dxp + 32 * c + i);
-                float* a = acc + 32 * c + i;
-                a[0] = fmaf(v.x, __uint_as_float(P[i]), a[0]);
-                a[1] = fmaf(v.y, __uint_as_float(P[i + 1]), a[1]);
-                a[2] = fmaf(v.z, __uint_as_float(P[i + 2]), a[2]);
-                a[3] = fmaf(v.w, __uint_as_float(P[i + 3]), a[3]);
-              }
+              fma_chunk(c, dxp, P);
             }
           });
         }
@@ -831,9 +826,12 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
     }
     if (!DOTS && ok && row_ok) {
 #pragma unroll
-      for (int i = 0; i < CPW; ++i) {
-        const int t = tok0 + cb * CPW + i;  // slice z's partials
-        if (t < nt) out[((size_t)blockIdx.z * nt + t) * od + row_g] = sigma * acc[i];
+      for (int i = 0; i < CPW / 2; ++i) {
+        const float2 v = upk2(acc[i]);
+        const int t = tok0 + cb * CPW + 2 * i;  // slice z's partials
+        float* o = out + ((size_t)blockIdx.z * nt + t) * od + row_g;
+        if (t < nt) o[0] = sigma * v.x;
+        if (t + 1 < nt) o[od] = sigma * v.y;
       }
     }
   }

@@ -103,6 +103,36 @@ __device__ __forceinline__ int fused_code_offset(int k) {
   return (((seg * 4 + ((r & 63) >> 4)) * 32 + (r >> 6)) << 4) + (r & 15);
 }
 
+// Lane-constant part of the Q4_K (scale, min) decode of sub-blocks 2p and
+// 2p+1 ("llama.cpp MMQ", sec. 6): pairs 0-1 keep both 6-bit codes in the low
+// six bits of scale bytes j and j+4; pairs 2-3 keep their low 4 bits in the
+// nibbles of bytes j+4 and their top 2 bits in the top of bytes j-4 / j.
+// With the header words w1..w3 holding scales[0..11] and sh = 16(p%2),
+//   p < 2:  sc2 = (w1 >> sh) & 0x3F3F,   m2 = (w2 >> sh) & 0x3F3F
+//   p >= 2: sc2 = ((w3 >> sh) & 0x0F0F) | ((w1 >> (sh+2)) & 0x3030)
+//           m2  = ((w3 >> (sh+4)) & 0x0F0F) | ((w2 >> (sh+2)) & 0x3030)
+// which one branch-free form covers with per-lane shifts and masks.
+struct Q4PairDecode {
+  uint32_t sh, sh2, shm, mA, mB;
+  bool upper;
+  __device__ explicit Q4PairDecode(int p)
+      : sh(16u * (uint32_t)(p & 1)), sh2(16u * (uint32_t)(p & 1) + 2u), shm(16u * (uint32_t)(p & 1) + (p >= 2 ? 4u : 0u)),
+        mA(p >= 2 ? 0x0F0Fu : 0x3F3Fu), mB(p >= 2 ? 0x3030u : 0u), upper(p >= 2) {}
+  // the two scale codes (bytes 0, 1) and the two min codes of the pair
+  __device__ __forceinline__ void codes(uint32_t w1, uint32_t w2, uint32_t w3, uint32_t& sc2, uint32_t& m2) const {
+    const uint32_t a = upper ? w3 : w1, am = upper ? w3 : w2;
+    sc2 = ((a >> sh) & mA) | ((w1 >> sh2) & mB);
+    m2 = ((am >> shm) & mA) | ((w2 >> sh2) & mB);
+  }
+};
+
+// 2^23 + byte b of w as an f32 bit pattern (b = 0 or 1): one PRMT, no
+// integer-to-float conversion; fma(s, f, -s * 2^23) is then s * byte exactly
+// whenever s * byte fits the f32 significand.
+__device__ __forceinline__ float magic_byte(uint32_t w, uint32_t b) {
+  return __uint_as_float(prmt(w, 0x4B000000u, 0x7650u + b));
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -237,6 +267,9 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
   } else if (nchunks > 0) {
     // ----------------------------------------------------------- consumers
     const int sbo = lane >> 2, p = lane & 3;
+    const Q4PairDecode q4d(p);
+    // this lane's first block in a stage: row warp*R of the stage, super-block sbo
+    const int lane_w = QT == kQ4 ? (warp * R) * C::SEG_BYTES + sbo * kQ4KBytes : 0;
     bool ok = true;
     // the preceding grid is complete before any consumer reads x or writes:
     // one warp waits for it, the others sleep on a named barrier meanwhile
@@ -278,15 +311,15 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
           for (int i = 0; i < w2; ++i) m[i] = fmaxf(m[i], m[i + w2]);
         const float amax = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
         const float d = __fdiv_rn(amax, 127.0f);
-        int q[16];
-        q8_codes<16>(v, d, q);
+        uint32_t cw[16];
+        q8_code_words<16>(v, d, cw);
+        // pack the codes and sum them (a signed-byte dp4a against ones)
         int sum = 0;
         uint32_t pk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          sum += q[4 * i] + q[4 * i + 1] + q[4 * i + 2] + q[4 * i + 3];
-          pk[i] = (uint32_t)(q[4 * i] & 0xFF) | ((uint32_t)(q[4 * i + 1] & 0xFF) << 8) |
-                  ((uint32_t)(q[4 * i + 2] & 0xFF) << 16) | ((uint32_t)(q[4 * i + 3] & 0xFF) << 24);
+          pk[i] = pack_low_bytes(cw[4 * i], cw[4 * i + 1], cw[4 * i + 2], cw[4 * i + 3]);
+          sum = __dp4a((int)pk[i], 0x01010101, sum);
         }
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         const float s = __fmul_rn(d, (float)sum);
@@ -325,7 +358,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
       if constexpr (QT == kQ4) {
       // the R weight rows of this lane: nibbles split into the low (sub-block
       // 2p) and high (sub-block 2p+1) planes, and the four scale factors
-      const uint8_t* stage = smem + st * stage_bytes;
+      const uint8_t* stage = smem + st * stage_bytes + lane_w;
       uint32_t lo[R][8], hi[R][8];
       float a_lo[R], a_hi[R], c_lo[R], c_hi[R];
 #pragma unroll
@@ -333,7 +366,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         const bool use = live && row0 + i < od;
         uint4 hdr = make_uint4(0, 0, 0, 0), q0 = hdr, q1 = hdr;
         if (use) {
-          const uint8_t* blk = stage + (warp * R + i) * C::SEG_BYTES + sbo * kQ4KBytes;
+          const uint8_t* blk = stage + i * C::SEG_BYTES;
           hdr = *reinterpret_cast<const uint4*>(blk);
           q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * p);
           q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * p);
@@ -345,12 +378,15 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
           hi[i][k] = w[k] & 0xF0F0F0F0u;  // 16 x the high nibbles: one AND instead of a shift and an AND
         }
         uint32_t sc2, m2;
-        q4k_pair_codes(hdr.y, hdr.z, hdr.w, p, sc2, m2);
-        const float d = half_bits_to_float(hdr.x), dmin = half_bits_to_float(hdr.x >> 16);
-        a_lo[i] = d * (float)(sc2 & 0xFFu);
-        a_hi[i] = d * (float)(sc2 >> 8) * 0.0625f;  // the high-nibble dot comes out 16x (exact power of 2)
-        c_lo[i] = dmin * (float)(m2 & 0xFFu);
-        c_hi[i] = dmin * (float)(m2 >> 8);
+        q4d.codes(hdr.y, hdr.z, hdr.w, sc2, m2);
+        const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));  // (d, dmin)
+        // d * sc and dmin * m are exact in f32; the high-nibble dot comes out
+        // 16x, so its factor carries 1/16 (an exact power of 2)
+        const float dq = dd.x * 0.0625f;
+        a_lo[i] = fmaf(dd.x, magic_byte(sc2, 0), -0x1p23f * dd.x);
+        a_hi[i] = fmaf(dq, magic_byte(sc2, 1), -0x1p23f * dq);
+        c_lo[i] = fmaf(dd.y, magic_byte(m2, 0), -0x1p23f * dd.y);
+        c_hi[i] = fmaf(dd.y, magic_byte(m2, 1), -0x1p23f * dd.y);
       }
       // the stage's words are in registers: hand it back before the dots
       release_stage(empty0 + 8 * st);

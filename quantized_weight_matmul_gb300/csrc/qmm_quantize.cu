@@ -42,7 +42,7 @@ __device__ __forceinline__ void write_gemm_scales(float* scl, int64_t nb, int64_
 // Eight lanes per 32-value block, four values per lane (one 16-byte load);
 // a warp takes four blocks per step, grid-stride over all nt*K/32 blocks.
 // The block maximum and the code sum are 3-step shuffle reductions within the
-// eight lanes; d = amax/127 by IEEE division, the codes by q8_codes (the
+// eight lanes; d = amax/127 by IEEE division, the codes by q8_code_words (the
 // same integers IEEE division and round-half-even give), s = d * sum(q).
 // When xh / scl are non-null the same pass also writes the tensor-core GEMM
 // operands (the workspace layout of qmm_internal.h): the codes as exact f16
@@ -71,18 +71,19 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restr
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const float d = __fdiv_rn(amax, 127.0f);
-    int q[4];
-    q8_codes<4>(v, d, q);
-    int sum = q[0] + q[1] + q[2] + q[3];
+    uint32_t cw[4];
+    q8_code_words<4>(v, d, cw);
+    const uint32_t pk = pack_low_bytes(cw[0], cw[1], cw[2], cw[3]);
+    int sum = __dp4a((int)pk, 0x01010101, 0);  // the four signed codes
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
     sum += __shfl_xor_sync(0xffffffffu, sum, 4);
     const float s = __fmul_rn(d, (float)sum);
     if (in) {
-      *reinterpret_cast<uint32_t*>(xq + b * 32 + 4 * q8) = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
-                                                            ((uint32_t)(q[2] & 0xFF) << 16) |
-                                                            ((uint32_t)(q[3] & 0xFF) << 24);
+      *reinterpret_cast<uint32_t*>(xq + b * 32 + 4 * q8) = pk;
       if (xh) {
+        const int q[4] = {(int)(int8_t)(cw[0] & 0xFFu), (int)(int8_t)(cw[1] & 0xFFu), (int)(int8_t)(cw[2] & 0xFFu),
+                          (int)(int8_t)(cw[3] & 0xFFu)};
         const __half2 h01 = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
         const __half2 h23 = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
         *reinterpret_cast<uint2*>(xh + b * 32 + 4 * q8) =
