@@ -36,7 +36,10 @@
 //               written straight into TMEM (tcgen05.st), where the MMA reads
 //               it as its A operand -- the operand never touches shared
 //               memory, whose bandwidth the MMAs' activation reads need.
-//   warps 8-15  epilogue, two per lane quarter (BN/2 token columns each):
+//               The 64-token Q6_K tile has eight (warps 4-11), two per lane
+//               quarter, each unpacking one 32-value block of every stage.
+//   8 warps     epilogue (warps 8-15, or 12-19), two per lane quarter
+//               (BN/2 token columns each):
 //               per accumulator the TMEM loads of its columns, the
 //               accumulator handed back after the last of them, the fp32
 //               rescale into register accumulators; one store at the end.
@@ -65,18 +68,23 @@ struct Cfg {
   static constexpr int KS = 64;                 // k per operand stage
   // first unpack warp; epilogue warps per TMEM lane quarter, all epilogue
   // warps, the first of them
-  static constexpr int U0 = 4, EPQ = 2, NE = 4 * EPQ, E0 = 8;
+  // Q6_K's unpack (two operands per code, realigned 2-byte blocks) costs
+  // several times Q4_K's, so the 64-token Q6_K tile, whose epilogue is light,
+  // gets two unpack warps per lane quarter, one per 32-value block of a stage
+  static constexpr int UW = (QT == kQ6 && BN == 64) ? 8 : 4;  // unpack warps
+  static constexpr int U0 = 4, EPQ = 2, NE = 4 * EPQ, E0 = U0 + UW;
   static constexpr int THREADS = 32 * (E0 + NE);
   static constexpr int CPW = BN / EPQ;  // token columns per epilogue warp
   static_assert(CPW % 32 == 0, "whole 32-column TMEM loads");
   // register budgets per warpgroup: producers / MMA (warps 0-3), unpack
-  // (4-7), epilogue (8-).  The block is launched with 65536 / THREADS per
-  // thread, rounded down to a multiple of 8 (128 for 512 threads, 80 for
-  // 768); the budgets add up to no more than that.
+  // (U0 .. E0-1), epilogue (E0 ..).  The block is launched with 65536 /
+  // THREADS per thread, rounded down to a multiple of 8 (128 for 512
+  // threads, 96 for 640); the budgets add up to no more than that.
   static constexpr uint32_t REG_LAUNCH = (65536 / THREADS) & ~7u;
-  static constexpr uint32_t REG_CTL = THREADS == 512 ? 56 : 40, REG_UNPACK = THREADS == 512 ? 96 : 80;
-  static constexpr uint32_t REG_EPI = ((REG_LAUNCH * THREADS - 128 * (REG_CTL + REG_UNPACK)) / (32 * NE)) & ~7u;
-  static_assert(128 * (REG_CTL + REG_UNPACK) + 32 * NE * REG_EPI <= REG_LAUNCH * THREADS, "register split");
+  static constexpr uint32_t REG_CTL = 56, REG_UNPACK = THREADS == 512 ? 96 : 80;
+  static constexpr uint32_t REG_EPI =
+      ((REG_LAUNCH * THREADS - 128 * REG_CTL - 32 * UW * REG_UNPACK) / (32 * NE)) & ~7u;
+  static_assert(128 * REG_CTL + 32 * UW * REG_UNPACK + 32 * NE * REG_EPI <= REG_LAUNCH * THREADS, "register split");
   static_assert(REG_EPI >= REG_LAUNCH, "the epilogue gains registers");
   // ring depths: raw weight super-blocks, activation stages, dx stages,
   // operand stages in TMEM.  The activation ring is as deep as shared memory
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::RS; ++i) {
       mbar_init(bars.raw_full(i), 1);
-      mbar_init(bars.raw_empty(i), 4 + (MIN ? 1 : 0));  // unpack warps (+ the min-term MMAs)
+      mbar_init(bars.raw_empty(i), C::UW + (MIN ? 1 : 0));  // unpack warps (+ the min-term MMAs)
     }
     for (int i = 0; i < C::BS; ++i) {
       mbar_init(bars.b_full(i), 1);
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
       mbar_init(bars.dx_empty(i), C::NE);  // the epilogue warps read the stage's dx rows
     }
     for (int i = 0; i < C::AS; ++i) {
-      mbar_init(bars.a_full(i), 4);
+      mbar_init(bars.a_full(i), C::UW);
       mbar_init(bars.a_empty(i), 1);
     }
     for (int i = 0; i < C::NBUF; ++i) {
@@ -553,6 +561,9 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
     // ----------------------------------------------------------- unpack
     const int q = warp & 3;       // TMEM lane quarter
     const int r = 32 * q + lane;  // the thread's weight row within the tile
+    // Q6_K: the 32-value block of each stage this warp unpacks (both when
+    // there is one unpack warp per lane quarter)
+    const int blk0 = C::UW == 8 ? (warp - C::U0) >> 2 : 0, nblk = C::UW == 8 ? 1 : 2;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     int rs = 0;
     uint32_t rph = 0;  // parity of the raw ring's round
@@ -621,7 +632,9 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
           load_words_even<1>(row, blk_off + 192 + 4 * s, sw);  // the scales of groups 4s..4s+3
           const bool dz = (d6 & 0x7FFFu) == 0;
 #pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {
+          for (int bi = 0; bi < 2; ++bi) {
+            if (bi >= nblk) break;
+            const int blk = blk0 + bi;
             uint32_t L[8];
             load_words_even<8>(row, blk_off + 64 * n + 32 * blk, L);
             // groups 4s + 2blk and 4s + 2blk + 1: bytes 2blk, 2blk+1 of scale word s
