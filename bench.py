@@ -39,6 +39,8 @@ cpu_baseline  the CPU oracle (plain scalar C, all host cores) on the same step.
 --sweep            one JSON line per case of every workload family (or of
                    --shape QTYPE:ODxKxNT[,...]), timed as a per_nt record;
                    not the contract line.
+--profile SPEC     a fixed number (--calls) of eager calls of one case, for
+                   ncu captures; no timing.
 Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
 torch.distributed.run, one rank per GPU, each rank running the same workload on
 its own GPU (replicas; weak scaling).
@@ -66,10 +68,11 @@ NCOPIES = 16
 # ncu capture of the fused quantize + MMVQ kernel (nt = 1, 11008 x 4096): dram
 # read + write bytes per launch, and the hash of qmm_gemv.cu it was taken on.
 # Reported as roofline.traffic only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha1": "e8269341b0f9c83e84d35a4c6d5cf8ee33fa6538", "bytes_per_launch": 25408768}
+NCU_TRAFFIC = {"source_sha1": "c7f82e3ed2211298bf1a9504a6aee067f4274699", "bytes_per_launch": 25409664}
 # The same for the tensor-core GEMM (Q4_K 14336 x 4096, nt = 512; prepass and
 # GEMM kernel launches added), keyed on qmm_gemm_tc.cu.
-NCU_TRAFFIC_GEMM = {"source_sha1": "f7b301c8dc44372d334e667783df790db643cadf", "bytes_per_launch": 2639616 + 38114816 + 307456}
+NCU_TRAFFIC_GEMM = {"source_sha1": "6af0b12762c8ab53a5bb0a336d56b927a558937a",
+                    "bytes_per_launch": 2639616 + 38139904 + 915712}
 
 # The cases of the per_nt array: (qtype name, od, K, nt values).
 PER_NT = [("Q4_K", 4096, 4096, (1, 2, 4, 8, 16, 128, 512, 2048)),
@@ -700,6 +703,50 @@ def run_sweep(args):
     return 0
 
 
+def run_profile(args):
+    """A fixed number of eager calls of one case, for ncu captures (not a
+    timing): --profile QTYPE:ODxKxNT[:path|gemv|gemm] --calls N.  `path` is
+    qmm_matmul from f32 x (the decode route's fused kernel at nt <= 4), `gemv`
+    / `gemm` the matmul on q8_1 input; two weight copies alternate."""
+    import torch
+    import quantized_weight_matmul_gb300 as qmm
+    from quantized_weight_matmul_gb300 import synth
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    parts = args.profile.split(":")
+    qt, dims = parts[0], parts[1]
+    how = parts[2] if len(parts) > 2 else "path"
+    od, K, nt = (int(v) for v in dims.split("x"))
+    c = synth.Case({"Q4_K": synth.Q4_K, "Q6_K": synth.Q6_K}[qt], od, K, nt, outliers=True)
+    W, x = c.generate()
+    Ws = [torch.from_numpy(W).to(dev) for _ in range(2)]
+    xd = torch.from_numpy(x).to(dev)
+    xq, xds = qmm.quantize_q8_1(xd)
+    xq8 = torch.empty_like(xq)
+    xds8 = torch.empty_like(xds)
+    out = torch.empty((nt, od), dtype=torch.float32, device=dev)
+    need = max(qmm.qmm_matmul_workspace_bytes(c.qtype, od, K, nt), qmm.qmm_gemm_workspace_bytes(c.qtype, od, K, nt))
+    ws = qmm.workspace(need, dev)
+    s = torch.cuda.current_stream().cuda_stream
+    for k in range(args.calls):
+        w = Ws[k % 2].data_ptr()
+        if how == "path":
+            rc = qmm.qmm_matmul(c.qtype, w, xd.data_ptr(), xq8.data_ptr(), xds8.data_ptr(), out.data_ptr(), od, K,
+                                nt, ws.data_ptr(), need, qmm.QMM_FLAG_STATIC_WEIGHTS, s)
+        elif how == "gemv":
+            rc = qmm.qmm_gemv(c.qtype, w, xq.data_ptr(), xds.data_ptr(), out.data_ptr(), od, K, nt, s)
+        else:
+            rc = qmm.qmm_gemm(c.qtype, w, xq.data_ptr(), xds.data_ptr(), out.data_ptr(), od, K, nt, ws.data_ptr(),
+                              need, s)
+        if rc != qmm.QMM_OK:
+            raise qmm.QmmError(rc, how)
+    torch.cuda.synchronize()
+    if qmm.qmm_sync_status(s) != qmm.QMM_OK:
+        raise RuntimeError("device status word set")
+    print(json.dumps({"profile": args.profile, "calls": args.calls}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -714,11 +761,15 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-nt", action="store_true", help="leave out the per_nt array and roofline_gemm")
+    ap.add_argument("--profile", default="", help="QTYPE:ODxKxNT[:path|gemv|gemm]: eager calls for ncu, no timing")
+    ap.add_argument("--calls", type=int, default=6, help="--profile: number of calls")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
     if args.sweep:
         return run_sweep(args)
     return run_gpu(args)

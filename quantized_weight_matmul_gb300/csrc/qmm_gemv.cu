@@ -361,15 +361,25 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
       const uint8_t* stage = smem + st * stage_bytes + lane_w;
       uint32_t lo[R][8], hi[R][8];
       float a_lo[R], a_hi[R], c_lo[R], c_hi[R];
+      // a whole stage -- all R rows in the matrix, the segment's 8 super-
+      // blocks in the row -- takes unpredicated loads (every stage but the
+      // last of a ragged matrix)
+      const bool whole = row0 + R <= od && (seg + 1) * kSegSB <= nsb;
 #pragma unroll
       for (int i = 0; i < R; ++i) {
-        const bool use = live && row0 + i < od;
-        uint4 hdr = make_uint4(0, 0, 0, 0), q0 = hdr, q1 = hdr;
-        if (use) {
-          const uint8_t* blk = stage + i * C::SEG_BYTES;
+        uint4 hdr, q0, q1;
+        const uint8_t* blk = stage + i * C::SEG_BYTES;
+        if (whole) {
           hdr = *reinterpret_cast<const uint4*>(blk);
           q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * p);
           q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * p);
+        } else {
+          hdr = q0 = q1 = make_uint4(0, 0, 0, 0);
+          if (live && row0 + i < od) {
+            hdr = *reinterpret_cast<const uint4*>(blk);
+            q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * p);
+            q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * p);
+          }
         }
         const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
