@@ -328,6 +328,24 @@ __device__ __forceinline__ void load_words_even(const uint8_t* base, int off, ui
   }
 }
 
+// The same words without a branch: N + 1 aligned words are read whatever the
+// offset, and each output takes its bytes through a PRMT whose selector
+// depends on the offset -- for lanes of one warp whose offsets differ in
+// alignment (a branch would run both paths one after the other).  Reads one
+// word past the N that an aligned offset needs; the caller's row must hold it.
+template <int N>
+__device__ __forceinline__ void load_words_even_bf(const uint8_t* base, int off, uint32_t (&out)[N]) {
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(base + (off & ~3));
+  const uint32_t sel = (off & 2) ? 0x5432u : 0x3210u;
+  uint32_t prev = p[0];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const uint32_t nxt = p[i + 1];
+    out[i] = prmt(prev, nxt, sel);
+    prev = nxt;
+  }
+}
+
 // Rows whose pitch is not a multiple of 16 bytes (Q6_K with K % 2048 != 0)
 // cannot be described by a TMA tensor map; they are staged row by row as
 // the 16-byte-aligned window [start & ~15, (end + 15) & ~15) around the bytes

@@ -467,10 +467,14 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
           // even: the row's blocks start at its window's offset (0 for TMA boxes)
           const int boff = (row_copy ? (int)(((size_t)(row0 + i) * row_bytes + (size_t)seg * C::SEG_BYTES) & 15) : 0) +
                            sbo * kQ6KBytes;
-          load_words_even<8>(rowp, boff + 64 * n, L0);
-          load_words_even<8>(rowp, boff + 64 * n + 32, L1);
-          load_words_even<8>(rowp, boff + 128 + 32 * n, H);
-          load_words_even<1>(rowp, boff + 192 + 4 * p, sw);
+          // (the lanes' blocks alternate between 4- and 2-byte alignment:
+          // branch-free realignment; the extra word each run reads stays
+          // inside the stage row -- the last one, of the scale word of block
+          // 7, ends on the row's last byte)
+          load_words_even_bf<8>(rowp, boff + 64 * n, L0);
+          load_words_even_bf<8>(rowp, boff + 64 * n + 32, L1);
+          load_words_even_bf<8>(rowp, boff + 128 + 32 * n, H);
+          load_words_even_bf<1>(rowp, boff + 192 + 4 * p, sw);
           dbits = *reinterpret_cast<const uint16_t*>(rowp + boff + 208);
         }
 #pragma unroll
