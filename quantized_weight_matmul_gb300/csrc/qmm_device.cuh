@@ -283,15 +283,6 @@ __device__ __forceinline__ void q8_code_words(const float (&v)[N], float d, uint
   }
 }
 
-// The same codes as signed integers.
-template <int N>
-__device__ __forceinline__ void q8_codes(const float (&v)[N], float d, int (&q)[N]) {
-  uint32_t c[N];
-  q8_code_words<N>(v, d, c);
-#pragma unroll
-  for (int i = 0; i < N; ++i) q[i] = (int)(int8_t)(c[i] & 0xFFu);
-}
-
 // The low bytes of four words, packed in order into one word.
 __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   uint32_t ab, cd, r;

@@ -27,7 +27,7 @@
 //     once per CTA into shared memory (bulk copy);
 //   * fused: the consumer warps quantize the f32 activations themselves into
 //     shared memory (two lanes per 32-value block; the same codes as the
-//     quantizer, see q8_codes) and write the q8_1 outputs too -- one kernel
+//     quantizer, see q8_code_words) and write the q8_1 outputs too -- one kernel
 //     per matmul instead of two, for the decode shapes where nt*K is small.
 // Kernels are launched as programmatic dependents of the preceding kernel
 // and let their own dependents start early, so consecutive matmuls overlap
@@ -468,9 +468,10 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
           const int boff = (row_copy ? (int)(((size_t)(row0 + i) * row_bytes + (size_t)seg * C::SEG_BYTES) & 15) : 0) +
                            sbo * kQ6KBytes;
           // (the lanes' blocks alternate between 4- and 2-byte alignment:
-          // branch-free realignment; the extra word each run reads stays
-          // inside the stage row -- the last one, of the scale word of block
-          // 7, ends on the row's last byte)
+          // branch-free realignment.  The extra word each run reads stays
+          // inside the stage row: the furthest, after the scale word of block
+          // 7, ends on byte 1680 of a 1680-byte TMA row, or at most 14 bytes
+          // later inside the 32 spare bytes of a row staged as a window)
           load_words_even_bf<8>(rowp, boff + 64 * n, L0);
           load_words_even_bf<8>(rowp, boff + 64 * n + 32, L1);
           load_words_even_bf<8>(rowp, boff + 128 + 32 * n, H);
