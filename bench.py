@@ -68,7 +68,7 @@ NCOPIES = 16
 # ncu capture of the fused quantize + MMVQ kernel (nt = 1, 11008 x 4096): dram
 # read + write bytes per launch, and the hash of qmm_gemv.cu it was taken on.
 # Reported as roofline.traffic only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha1": "703c8ebc80ea1bfc4f2d774512b538245a2f3f7f", "bytes_per_launch": 25407872}
+NCU_TRAFFIC = {"source_sha1": "881c73e5d44544a9e07780d779149b4ebb63ffb4", "bytes_per_launch": 25407872}
 # The same for the tensor-core GEMM (Q4_K 14336 x 4096, nt = 512; prepass and
 # GEMM kernel launches added), keyed on qmm_gemm_tc.cu.
 NCU_TRAFFIC_GEMM = {"source_sha1": "6af0b12762c8ab53a5bb0a336d56b927a558937a",
