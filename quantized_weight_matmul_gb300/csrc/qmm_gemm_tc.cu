@@ -628,15 +628,27 @@ __global__ void __launch_bounds__(Cfg<QT, BN>::THREADS, 1)
         } else {
           const int n = s >> 1;
           uint32_t H[8], sw[1];
-          load_words_even<8>(row, blk_off + 128 + 32 * n, H);
-          load_words_even<1>(row, blk_off + 192 + 4 * s, sw);  // the scales of groups 4s..4s+3
+          // TMA rows share one block offset (a warp-uniform branch); rows
+          // staged as windows each have their own, so their lanes' words
+          // differ in alignment: branch-free reads there (the extra word read
+          // ends by byte 224 of the 240-byte row)
+          if (!row_copy) {
+            load_words_even<8>(row, blk_off + 128 + 32 * n, H);
+            load_words_even<1>(row, blk_off + 192 + 4 * s, sw);  // the scales of groups 4s..4s+3
+          } else {
+            load_words_even_bf<8>(row, blk_off + 128 + 32 * n, H);
+            load_words_even_bf<1>(row, blk_off + 192 + 4 * s, sw);
+          }
           const bool dz = (d6 & 0x7FFFu) == 0;
 #pragma unroll
           for (int bi = 0; bi < 2; ++bi) {
             if (bi >= nblk) break;
             const int blk = blk0 + bi;
             uint32_t L[8];
-            load_words_even<8>(row, blk_off + 64 * n + 32 * blk, L);
+            if (!row_copy)
+              load_words_even<8>(row, blk_off + 64 * n + 32 * blk, L);
+            else
+              load_words_even_bf<8>(row, blk_off + 64 * n + 32 * blk, L);
             // groups 4s + 2blk and 4s + 2blk + 1: bytes 2blk, 2blk+1 of scale word s
             uint32_t mh[2], ml[2];
 #pragma unroll

@@ -195,7 +195,12 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
 
   if (warp == NW) {
     // ----------------------------------------------------------- producer
-    if (lane == 0 && nchunks > 0) {
+    // Lane 0 waits for free stages and issues the copies.  Rows staged one by
+    // one (a row pitch that is not a multiple of 16 bytes) take one bulk copy
+    // per row: there the whole warp runs the loop and lane r stages row r of
+    // the stage, so that sixteen windows are computed and issued at once.
+    const unsigned am = row_copy ? 0xffffffffu : 1u;  // the lanes in the loop
+    if (nchunks > 0 && (lane == 0 || row_copy)) {
       if (!row_copy) prefetch_tmap(&tmW);
       if (!static_w) griddep_wait();
       int issued = 0, st = 0, ph = 0, seg = 0, grp = g_begin;
@@ -204,37 +209,40 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
         if (c == stages && !act_issued) {
           // the first stages of weights are in flight; now the activations,
           // which the preceding kernel may still be writing
-          griddep_wait();
-          mbar_arrive_expect_tx(act_bar, (uint32_t)act_bytes);
-          bulk_load(sb + act_off, xq, (uint32_t)act_q, act_bar);
-          bulk_load(sb + act_off + act_q, xds, (uint32_t)(act_bytes - act_q), act_bar);
+          if (lane == 0) {
+            griddep_wait();
+            mbar_arrive_expect_tx(act_bar, (uint32_t)act_bytes);
+            bulk_load(sb + act_off, xq, (uint32_t)act_q, act_bar);
+            bulk_load(sb + act_off + act_q, xds, (uint32_t)(act_bytes - act_q), act_bar);
+          }
           act_issued = true;
         }
-        if (!wait_bar(empty0 + 8 * st, ph ^ 1, g)) break;
+        if (!__all_sync(am, wait_bar(empty0 + 8 * st, ph ^ 1, g))) break;
         if (!(skip_first && c == 0)) {  // the stall test hook skips the first stage
           if (!row_copy) {
             mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE_BYTES);
             tma_load_2d(sb + st * C::STAGE_BYTES, &tmW, seg * (C::SEG_BYTES / 8), grp * C::CR, full0 + 8 * st);
           } else {
-            // the stage's super-blocks of each of its rows, one window per row
+            // the stage's super-blocks of row `lane`, one window
             const int nbs = min(kSegSB, nsb - seg * kSegSB);
             const size_t total = (size_t)od * row_bytes;
-            uint32_t bytes = 0;
-            for (int r = 0; r < C::CR && grp * C::CR + r < od; ++r) {
-              const size_t start = (size_t)(grp * C::CR + r) * row_bytes + (size_t)seg * C::SEG_BYTES;
+            size_t a0 = 0, a1 = 0;
+            if (lane < C::CR && grp * C::CR + lane < od) {
+              const size_t start = (size_t)(grp * C::CR + lane) * row_bytes + (size_t)seg * C::SEG_BYTES;
               const RowWindow w = stage_row_window(start, start + (size_t)nbs * C::BLK, total,
-                                                   smem + st * stage_bytes + r * srow, W);
-              if (w.a1 > w.a0) bytes += (uint32_t)(w.a1 - w.a0);
+                                                   smem + st * stage_bytes + lane * srow, W);
+              a0 = w.a0;
+              a1 = w.a1 > w.a0 ? w.a1 : w.a0;
             }
-            mbar_arrive_expect_tx(full0 + 8 * st, bytes);
-            for (int r = 0; r < C::CR && grp * C::CR + r < od; ++r) {
-              const size_t start = (size_t)(grp * C::CR + r) * row_bytes + (size_t)seg * C::SEG_BYTES;
-              const size_t a0 = start & ~(size_t)15;
-              size_t a1 = (start + (size_t)nbs * C::BLK + 15) & ~(size_t)15;
-              if (a1 > (total & ~(size_t)15)) a1 = total & ~(size_t)15;
-              if (a1 > a0)
-                bulk_load(sb + st * stage_bytes + r * srow, W + a0, (uint32_t)(a1 - a0), full0 + 8 * st);
-            }
+            uint32_t bytes = (uint32_t)(a1 - a0);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+            // the bytes a lane stored itself (past the matrix's last 16-byte
+            // boundary) are ordered before lane 0's arrive by the warp sync
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, bytes);
+            __syncwarp();
+            if (a1 > a0) bulk_load(sb + st * stage_bytes + lane * srow, W + a0, (uint32_t)(a1 - a0), full0 + 8 * st);
           }
         }
         ++issued;
@@ -247,22 +255,24 @@ __global__ void __launch_bounds__(32 * (NW + 1), FUSED ? 2 : 1)
           ++grp;
         }
       }
-      if (!act_issued) {
-        griddep_wait();
-        mbar_arrive_expect_tx(act_bar, (uint32_t)act_bytes);
-        bulk_load(sb + act_off, xq, (uint32_t)act_q, act_bar);
-        bulk_load(sb + act_off + act_q, xds, (uint32_t)(act_bytes - act_q), act_bar);
+      if (lane == 0) {
+        if (!act_issued) {
+          griddep_wait();
+          mbar_arrive_expect_tx(act_bar, (uint32_t)act_bytes);
+          bulk_load(sb + act_off, xq, (uint32_t)act_q, act_bar);
+          bulk_load(sb + act_off + act_q, xds, (uint32_t)(act_bytes - act_q), act_bar);
+        }
+        // drain: every copy in flight lands before the CTA exits
+        const uint64_t dl = global_ns() + 1000000000ull;
+        for (int i = issued - stages; i < issued; ++i) {
+          if (i < 0 || (skip_first && i == 0)) continue;
+          for (uint32_t it = 0; !mbar_try_wait(full0 + 8 * (i % stages), (i / stages) & 1); ++it)
+            if ((it & 63u) == 63u && global_ns() > dl) break;
+        }
+        if (!FUSED)
+          for (uint32_t it = 0; !mbar_try_wait(act_bar, 0); ++it)
+            if ((it & 63u) == 63u && global_ns() > dl) break;
       }
-      // drain: every copy in flight lands before the CTA exits
-      const uint64_t dl = global_ns() + 1000000000ull;
-      for (int i = issued - stages; i < issued; ++i) {
-        if (i < 0 || (skip_first && i == 0)) continue;
-        for (uint32_t it = 0; !mbar_try_wait(full0 + 8 * (i % stages), (i / stages) & 1); ++it)
-          if ((it & 63u) == 63u && global_ns() > dl) break;
-      }
-      if (!FUSED)
-        for (uint32_t it = 0; !mbar_try_wait(act_bar, 0); ++it)
-          if ((it & 63u) == 63u && global_ns() > dl) break;
     }
   } else if (nchunks > 0) {
     // ----------------------------------------------------------- consumers

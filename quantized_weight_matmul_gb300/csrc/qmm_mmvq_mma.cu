@@ -523,8 +523,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kNW) {
     // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      const bool row_copy = mma_row_copy(QT, K);
+    // Lane 0 issues the copies.  Rows staged one by one (Q6_K rows whose
+    // pitch is not a multiple of 16 bytes) take one bulk copy per row: there
+    // the whole warp runs the weight stream and lane r stages row r.
+    const bool row_copy = mma_row_copy(QT, K);
+    const unsigned am = row_copy ? 0xffffffffu : 1u;  // the lanes issuing weights
+    if (lane == 0 || row_copy) {
       const int pitch = mma_pitch(QT, K), stage_sz = kTileRows * pitch;
       const size_t row_bytes = (size_t)nsb * C::BLK, total = (size_t)od * row_bytes;
       if (!row_copy) prefetch_tmap(&tmW);
@@ -532,29 +536,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one box: 16 rows x PITCH bytes from super-block 8*seg (rows past od
       // and bytes past the row's end arrive zero-filled)
       auto issue = [&]() -> bool {
-        if (!wait_bar(empty0 + 8 * st, ph ^ 1, gd)) return false;
+        if (!__all_sync(am, wait_bar(empty0 + 8 * st, ph ^ 1, gd))) return false;
         if (!(skip_first && issued == 0)) {  // the stall test hook skips the first stage
           if (!row_copy) {
             mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::STAGE);
             tma_load_2d(sb + st * C::STAGE, &tmW, seg * (C::SEG / 8), tile * kTileRows, full0 + 8 * st);
           } else {
-            // the stage's super-blocks of each of its rows, one window per row
+            // the stage's super-blocks of row `lane`, one window
             const int nbs = min(kSegSB, nsb - seg * kSegSB);
-            uint32_t bytes = 0;
-            for (int r = 0; r < kTileRows && tile * kTileRows + r < od; ++r) {
-              const size_t start = (size_t)(tile * kTileRows + r) * row_bytes + (size_t)seg * C::SEG;
+            size_t a0 = 0, a1 = 0;
+            if (lane < kTileRows && tile * kTileRows + lane < od) {
+              const size_t start = (size_t)(tile * kTileRows + lane) * row_bytes + (size_t)seg * C::SEG;
               const RowWindow w = stage_row_window(start, start + (size_t)nbs * C::BLK, total,
-                                                   smem + st * stage_sz + r * pitch, W);
-              if (w.a1 > w.a0) bytes += (uint32_t)(w.a1 - w.a0);
+                                                   smem + st * stage_sz + lane * pitch, W);
+              a0 = w.a0;
+              a1 = w.a1 > w.a0 ? w.a1 : w.a0;
             }
-            mbar_arrive_expect_tx(full0 + 8 * st, bytes);
-            for (int r = 0; r < kTileRows && tile * kTileRows + r < od; ++r) {
-              const size_t start = (size_t)(tile * kTileRows + r) * row_bytes + (size_t)seg * C::SEG;
-              const size_t a0 = start & ~(size_t)15;
-              size_t a1 = (start + (size_t)nbs * C::BLK + 15) & ~(size_t)15;
-              if (a1 > (total & ~(size_t)15)) a1 = total & ~(size_t)15;
-              if (a1 > a0) bulk_load(sb + st * stage_sz + r * pitch, W + a0, (uint32_t)(a1 - a0), full0 + 8 * st);
-            }
+            uint32_t bytes = (uint32_t)(a1 - a0);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+            // the bytes a lane stored itself (past the matrix's last 16-byte
+            // boundary) are ordered before lane 0's arrive by the warp sync
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, bytes);
+            __syncwarp();
+            if (a1 > a0) bulk_load(sb + st * stage_sz + lane * pitch, W + a0, (uint32_t)(a1 - a0), full0 + 8 * st);
           }
         }
         ++issued;
@@ -574,23 +580,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // copied next do not queue behind a full ring
       const int pre = static_w ? min(kPreStages, nitems) : 0;
       for (int i = 0; i < pre && pok; ++i) pok = issue();
+      // every lane that copies weights waits for the preceding grid from here
       griddep_wait();
-      // the activations: each token's codes (x16: into the upper half of its
-      // row), then all (d, s) pairs into the staging area
-      mbar_arrive_expect_tx(xbar, (uint32_t)(nt * K + nt * nbk * 8));
-      for (int t = 0; t < nt; ++t)
-        bulk_load(sb + P.x_off + t * P.xpitch + (X16 ? K + 64 : 0), xq + (size_t)t * K, (uint32_t)K, xbar);
-      bulk_load(sb + P.coef_off, xds, (uint32_t)(nt * nbk * 8), xbar);
+      if (lane == 0) {
+        // the activations: each token's codes (x16: into the upper half of its
+        // row), then all (d, s) pairs into the staging area
+        mbar_arrive_expect_tx(xbar, (uint32_t)(nt * K + nt * nbk * 8));
+        for (int t = 0; t < nt; ++t)
+          bulk_load(sb + P.x_off + t * P.xpitch + (X16 ? K + 64 : 0), xq + (size_t)t * K, (uint32_t)K, xbar);
+        bulk_load(sb + P.coef_off, xds, (uint32_t)(nt * nbk * 8), xbar);
+      }
       while (pok && issued < nitems) pok = issue();
-      // drain: every copy in flight lands before the CTA exits
-      const uint64_t dl = global_ns() + 1000000000ull;
-      for (int i = issued - stages; i < issued; ++i) {
-        if (i < 0 || (skip_first && i == 0)) continue;
-        for (uint32_t k = 0; !mbar_try_wait(full0 + 8 * (i % stages), (i / stages) & 1); ++k)
+      if (lane == 0) {
+        // drain: every copy in flight lands before the CTA exits
+        const uint64_t dl = global_ns() + 1000000000ull;
+        for (int i = issued - stages; i < issued; ++i) {
+          if (i < 0 || (skip_first && i == 0)) continue;
+          for (uint32_t k = 0; !mbar_try_wait(full0 + 8 * (i % stages), (i / stages) & 1); ++k)
+            if ((k & 63u) == 63u && global_ns() > dl) break;
+        }
+        for (uint32_t k = 0; !mbar_try_wait(xbar, 0); ++k)
           if ((k & 63u) == 63u && global_ns() > dl) break;
       }
-      for (uint32_t k = 0; !mbar_try_wait(xbar, 0); ++k)
-        if ((k & 63u) == 63u && global_ns() > dl) break;
     }
   } else if (nitems > 0) {
     consume<QT, NTL, X16, DOTS>(smem, P, out, dots, od, K, nt, stages, t_begin, nitems, full0, empty0, red0, xbar,
