@@ -68,11 +68,11 @@ NCOPIES = 16
 # ncu capture of the fused quantize + MMVQ kernel (nt = 1, 11008 x 4096): dram
 # read + write bytes per launch, and the hash of qmm_gemv.cu it was taken on.
 # Reported as roofline.traffic only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha1": "881c73e5d44544a9e07780d779149b4ebb63ffb4", "bytes_per_launch": 25407872}
+NCU_TRAFFIC = {"source_sha1": "c6330c3519319f3888d9005d5a05a9359afe021f", "bytes_per_launch": 25408256}
 # The same for the tensor-core GEMM (Q4_K 14336 x 4096, nt = 512; prepass and
 # GEMM kernel launches added), keyed on qmm_gemm_tc.cu.
-NCU_TRAFFIC_GEMM = {"source_sha1": "6af0b12762c8ab53a5bb0a336d56b927a558937a",
-                    "bytes_per_launch": 2639616 + 38139904 + 915712}
+NCU_TRAFFIC_GEMM = {"source_sha1": "768f14d907062ea2d9a3bcbe55ad9bad7d06e4cb",
+                    "bytes_per_launch": 2639616 + 38106112 + 951808}
 
 # The cases of the per_nt array: (qtype name, od, K, nt values).
 PER_NT = [("Q4_K", 4096, 4096, (1, 2, 4, 8, 16, 128, 512, 2048)),
