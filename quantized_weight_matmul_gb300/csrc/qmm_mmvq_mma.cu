@@ -30,11 +30,11 @@
 // Work split: a persistent grid of one CTA per SM, each owning a balanced
 // range of 16-row tiles.  A producer warp streams every tile in stages of 16
 // rows x 2048 k (one TMA box per stage, in a bank-conflict-free row pitch);
-// the sixteen consumer warps take one sixteenth of a stage's k each (Q4_K:
-// half a super-block; Q6_K: two quads of one half of each of two adjacent
-// super-blocks, so every warp meets one 4-byte- and one 2-byte-aligned block)
-// and add their partial sums at the end of a tile through shared memory in a
-// fixed order.
+// eight consumer warps take one eighth of a stage's k each (Q4_K: one
+// super-block; Q6_K: one half of each of two adjacent super-blocks, so every
+// warp meets 4-byte- and 2-byte-aligned blocks; sixteen warps for Q4_K with
+// raw activations, half a super-block each) and add their partial sums at
+// the end of a tile through shared memory in a fixed order.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -49,13 +49,20 @@ namespace {
 constexpr int kQ4 = 0, kQ6 = 1;
 constexpr int kSegSB = 8;      // super-blocks per stage (2048 k)
 constexpr int kTileRows = 16;  // one m16 tile
-constexpr int kNW = 16;        // consumer warps
-constexpr int kThreads = 32 * (kNW + 1);
 constexpr int kMaxStages = 8;
 constexpr int kPreStages = 2;  // weight stages a CTA may request before the activations are ready
-constexpr int kCoefRow = 80;   // bytes per row of a warp's coefficient table (4 x 16 + 16: no bank conflicts)
 constexpr int kRedRow = 130;   // floats per (warp, token tile) of the tile-sum buffer (128 + 2: no bank conflicts)
 constexpr int kSmemLimit = 227 * 1024;
+
+// Consumer warps.  A stage holds 32 (super-block, 64-value pair) units of
+// work; eight warps (four units each) take fewer instructions per stage than
+// sixteen and measured faster, except for Q4_K with raw int8 activations,
+// whose per-use conversion favours the wider split.
+__host__ __device__ constexpr int mma_warps(int qt, int x16) { return qt == kQ4 && !x16 ? 16 : 8; }
+__host__ __device__ constexpr int mma_threads(int qt, int x16) { return 32 * (mma_warps(qt, x16) + 1); }
+// bytes per row of a warp's coefficient table: one 16-byte entry per block
+// of the warp's units, plus 16 (no bank conflicts for the rows g = 0..7)
+__host__ __device__ constexpr int mma_coef_row(int nw) { return 64 * 16 / nw + 16; }
 
 template <int QT>
 struct MC {
@@ -102,10 +109,13 @@ __host__ __device__ inline Plan make_plan(int qt, int ntl, int nt, int K, int st
   p.tab_off = p.x_off + ((nt * p.xpitch + 127) & ~127);
   const int tab_bytes = (K / 32) * 4 * ntl * (qt == kQ4 ? 16 : 32);
   p.coef_off = p.tab_off + tab_bytes;
-  p.red_off = p.coef_off + kNW * kTileRows * kCoefRow;
-  p.bar_off = p.red_off + ((2 * kNW * ntl * kRedRow * 4 + 15) & ~15);
+  const int nw = mma_warps(qt, x16);
+  p.red_off = p.coef_off + nw * kTileRows * mma_coef_row(nw);
+  // the raw (d, s) pairs are staged from coef_off on: the area ends past
+  // the tile-sum buffer and past them
+  const int pair_end = p.coef_off + nt * (K / 32) * 8, red_end = p.red_off + 2 * nw * ntl * kRedRow * 4;
+  p.bar_off = ((pair_end > red_end ? pair_end : red_end) + 15) & ~15;
   p.total = p.bar_off + (2 * stages + 5) * 8 + 16;
-  if (nt * (K / 32) * 8 > p.bar_off - p.coef_off) p.total = 1 << 30;  // no room to stage the (d, s) pairs
   return p;
 }
 
@@ -148,7 +158,9 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
                                         int nitems, uint32_t full0, uint32_t empty0, uint32_t red0, uint32_t xbar,
                                         const Guard& gd) {
   using C = MC<QT>;
-  constexpr int CT = 32 * kNW;  // consumer threads
+  constexpr int kNW = mma_warps(QT, X16), CT = 32 * kNW;  // consumer warps, threads
+  constexpr int kUPW = 32 / kNW;                           // units of a stage per warp
+  constexpr int kCoefRow = mma_coef_row(kNW);
   const int nsb = K >> 8, nbk = K >> 5, nseg = (nsb + kSegSB - 1) / kSegSB;
   const int np = 4 * NTL;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -261,20 +273,22 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
   // Fixed-order sum of the warps' partials of finished tile `to` (rows from
   // tr0), once all warps have written them; done one stage later than the
   // write, so that no warp waits for the slowest one at a tile boundary.
-  // Thread T adds warps 4q..4q+3 (q = (lane >> 3) & 3) for output o, then
-  // the quad's partial sums meet by two shuffles: ((w0..3 + w4..7) + ...).
+  // A warp owns OPW of the 128 outputs of a token tile; thread T adds warps
+  // 4q..4q+3 (q = lane / OPW) for output o, then the partial sums of the q's
+  // meet by shuffles in a fixed order: ((w0..3 + w4..7) + (w8..11 + w12..15)).
+  constexpr int OPW = 128 / kNW;
   auto reduce_tile = [&](int to, int tr0) -> bool {
     const int par = to & 1;
     if (!__all_sync(0xffffffffu, wait_bar(red0 + 8 * par, (to >> 1) & 1, gd))) return false;
     const float* red = red_base + par * (kNW * NTL * kRedRow);
-    const int q = lane >> 3, o = 8 * warp + (lane & 7);
+    const int q = lane / OPW, o = OPW * warp + lane % OPW;
 #pragma unroll
     for (int n = 0; n < NTL; ++n) {
       float sum = 0.f;
 #pragma unroll
       for (int w = 0; w < 4; ++w) sum += red[((4 * q + w) * NTL + n) * kRedRow + o];
-      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+#pragma unroll
+      for (int m = OPW; m < 32; m <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
       const int ln = o >> 2, e = o & 3;
       const int row = tr0 + (ln >> 2) + 8 * (e >> 1), t = 8 * n + 2 * (ln & 3) + (e & 1);
       if (q == 0 && row < od && t < nt) out[(size_t)t * od + row] = sum;
@@ -295,28 +309,33 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
       return row_copy ? (int)(((size_t)(r0 + r) * row_bytes + (size_t)seg * C::SEG) & 15) : 0;
     };
     if constexpr (QT == kQ4) {
-      // warp -> super-block warp/2 of the stage, block pairs 2(warp&1) and 2(warp&1)+1
-      const int sbl = warp >> 1, ps = warp & 1, sbi = seg * kSegSB + sbl;
+      // warp -> super-block sbl of the stage, block pairs p0 .. p0 + kUPW - 1
+      constexpr int WPS = 4 / kUPW;  // warps per super-block
+      const int sbl = warp / WPS, p0 = (warp % WPS) * kUPW, sbi = seg * kSegSB + sbl;
       if (sbi < nsb) {
-        {  // coefficients, 16 rows x 4 sub-blocks: lane -> row lane/2, pair 2ps + (lane&1)
-          const int row = lane >> 1, p = 2 * ps + (lane & 1);
+        {  // coefficients, 16 rows x kUPW pairs: lane -> row lane/2, pairs p0 + 2i + (lane&1)
+          const int row = lane >> 1;
           const uint4 hdr = *reinterpret_cast<const uint4*>(stage + row * C::PITCH + sbl * kQ4KBytes);
           const float d = half_bits_to_float(hdr.x), dmin = half_bits_to_float(hdr.x >> 16);
-          uint32_t sc2, m2;
-          q4k_pair_codes(hdr.y, hdr.z, hdr.w, p, sc2, m2);
-          // D comes out as 2^-24 (low nibbles) or 2^-20 (high nibbles) x the dot
-          const float clo = d * 0x1p24f * (float)(sc2 & 0xFFu), mlo = -dmin * (float)(m2 & 0xFFu);
-          const float chi = d * 0x1p20f * (float)(sc2 >> 8), mhi = -dmin * (float)(m2 >> 8);
-          float4* cr = reinterpret_cast<float4*>(coef + row * kCoefRow + 32 * (lane & 1));
-          cr[0] = make_float4(clo, clo, mlo, mlo);
-          cr[1] = make_float4(chi, chi, mhi, mhi);
+#pragma unroll
+          for (int i = 0; i < kUPW / 2; ++i) {
+            const int pp = 2 * i + (lane & 1);
+            uint32_t sc2, m2;
+            q4k_pair_codes(hdr.y, hdr.z, hdr.w, p0 + pp, sc2, m2);
+            // D comes out as 2^-24 (low nibbles) or 2^-20 (high nibbles) x the dot
+            const float clo = d * 0x1p24f * (float)(sc2 & 0xFFu), mlo = -dmin * (float)(m2 & 0xFFu);
+            const float chi = d * 0x1p20f * (float)(sc2 >> 8), mhi = -dmin * (float)(m2 >> 8);
+            float4* cr = reinterpret_cast<float4*>(coef + row * kCoefRow + 32 * pp);
+            cr[0] = make_float4(clo, clo, mlo, mlo);
+            cr[1] = make_float4(chi, chi, mhi, mhi);
+          }
         }
         __syncwarp();
         const uint8_t* bg = stage + g * C::PITCH + sbl * kQ4KBytes + 16 + 8 * c;
         const uint8_t* bh = bg + 8 * C::PITCH;
 #pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-          const int p = 2 * ps + pp;
+        for (int pp = 0; pp < kUPW; ++pp) {
+          const int p = p0 + pp;
           const uint2 wg = *reinterpret_cast<const uint2*>(bg + 32 * p);
           const uint2 wh = *reinterpret_cast<const uint2*>(bh + 32 * p);
           const uint32_t g0s = wg.x >> 8, g1s = wg.y >> 8, h0s = wh.x >> 8, h1s = wh.y >> 8;
@@ -351,23 +370,30 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
         }
       }
     } else {
-      // Q6_K: warp -> super-blocks 2k and 2k+1 (k = warp/4), half h, quads
-      // 2qp and 2qp+1 of that half: four blocks, two of each alignment
-      const int k2 = 2 * (warp >> 2), h = (warp >> 1) & 1, qp = warp & 1;
+      // Q6_K: warp -> super-blocks k2 and k2+1, half h, quad pairs qp0 ..
+      // qp0 + QPW - 1 of that half (quads 2qp and 2qp+1): blocks of both
+      // alignments.  Quad pairs 0 and 1 read the same ql and qh words (low
+      // and high nibbles, other qh bits), loaded once for both.
+      constexpr int QPW = kUPW / 2, WPH = 2 / QPW;  // quad pairs per warp, warps per half
+      const int k2 = 2 * (warp / (2 * WPH)), h = (warp / WPH) & 1, qp0 = (warp % WPH) * QPW;
       // (super-blocks past the row's end, in a partial last stage, are skipped:
       // rows staged one by one carry the next row's bytes there, not zeros)
-      {  // coefficients, 16 rows x 4 blocks x 2 groups: lane -> row lane/2, super-block 2k + (lane&1)
+      {  // coefficients, 16 rows x 2 super-blocks x QPW quad pairs x 2 blocks
+         // x 2 groups: lane -> row lane/2, super-block k2 + (lane&1)
         const int row = lane >> 1, u = lane & 1;
         const uint8_t* rowp = stage + row * pitch;
         const int boff = row_shift(row) + (k2 + u) * kQ6KBytes;
-        const uint32_t sw = word_even(rowp, boff + 192 + 8 * h + 4 * qp);  // scales of groups 8h+4qp..+3
         const float d = half_bits_to_float(*reinterpret_cast<const uint16_t*>(rowp + boff + 208)) * 0x1p24f;
-        float v[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = d * (float)(int8_t)((sw >> (8 * i)) & 0xFFu);
-        float4* cr = reinterpret_cast<float4*>(coef + row * kCoefRow + 32 * u);
-        cr[0] = make_float4(v[0], v[0], v[1], v[1]);
-        cr[1] = make_float4(v[2], v[2], v[3], v[3]);
+        for (int qi = 0; qi < QPW; ++qi) {
+          const uint32_t sw = word_even(rowp, boff + 192 + 8 * h + 4 * (qp0 + qi));  // groups 8h+4qp..+3
+          float v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] = d * (float)(int8_t)((sw >> (8 * i)) & 0xFFu);
+          float4* cr = reinterpret_cast<float4*>(coef + row * kCoefRow + 16 * (4 * qi + 2 * u));
+          cr[0] = make_float4(v[0], v[0], v[1], v[1]);
+          cr[1] = make_float4(v[2], v[2], v[3], v[3]);
+        }
       }
       __syncwarp();
 #pragma unroll
@@ -377,7 +403,8 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
         const uint8_t* rg = stage + g * pitch;
         const uint8_t* rh = rg + 8 * pitch;
         const int boff = sbl * kQ6KBytes, sg = row_shift(g), sh = row_shift(g + 8);
-        // words of rows g and g+8 for steps s = 0, 1: ql of quads 2qp, 2qp+1; qh
+        // words of rows g and g+8 for steps s = 0, 1: ql at the half's two
+        // 32-byte offsets (quad q takes offset q & 1, nibble q >> 1); qh
         uint32_t QL[2][2][2], QH[2][2];
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
@@ -390,8 +417,9 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
           QH[1][s] = word_even(rh, sh + oh);
         }
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const int q = 2 * qp + qq, jl = 2 * u + qq, j = 8 * sbi + 4 * h + q;  // j: block within the row
+        for (int qx = 0; qx < 2 * QPW; ++qx) {
+          const int qi = qx >> 1, qq = qx & 1, qp = qp0 + qi;
+          const int q = 2 * qp + qq, jl = 4 * qi + 2 * u + qq, j = 8 * sbi + 4 * h + q;  // j: block within the row
           const ulonglong2 cg = *reinterpret_cast<const ulonglong2*>(coef + g * kCoefRow + 16 * jl);
           const ulonglong2 ch = *reinterpret_cast<const ulonglong2*>(coef + (g + 8) * kCoefRow + 16 * jl);
           // 6-bit codes of quad q: low 4 bits from ql (high nibbles for quads
@@ -483,7 +511,7 @@ __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __r
 }
 
 template <int QT, int NTL, bool X16, bool DOTS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(mma_threads(QT, X16), 1)
     mmvq_mma_kernel(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restrict__ W,
                     const int8_t* __restrict__ xq, const float* __restrict__ xds,
                     float* __restrict__ out, int32_t* __restrict__ dots, int od, int K, int nt, int stages,
@@ -506,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t xbar = red0 + 32;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.bar_off + (2 * stages + 5) * 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kNW = mma_warps(QT, X16);
   const Guard gd{abort_flag, status, global_ns() + (uint64_t)limit_ms * 1000000ull};
 
   if (threadIdx.x == 0) {
@@ -657,7 +686,7 @@ int launch_mma_cfg(const void* W, const int8_t* xq, const float* xds, float* out
   const int stall = stall_ms();
   int grid = nsm > 0 ? nsm : 152;
   if (grid > tiles) grid = (int)tiles;
-  return launch_ex(kern, dim3(grid), dim3(kThreads), (size_t)p.total + 1024, stream, pdl, m,
+  return launch_ex(kern, dim3(grid), dim3(mma_threads(QT, X16)), (size_t)p.total + 1024, stream, pdl, m,
                    static_cast<const uint8_t*>(W), xq, xds, out, dots,
                    (int)od, (int)K, (int)nt, p.stages, status, static_w ? 1 : 0, stall > 0 ? stall : 4000,
                    stall > 0 ? 1 : 0);
