@@ -149,9 +149,9 @@ __device__ __forceinline__ uint32_t word_even(const uint8_t* row, int off) {
 }
 
 // The consumer warps: the activations (copied in by the producer) into their
-// operand layout once, then per stage the warp's sixteenth of the k range of
-// one 16-row tile, and one stage after a tile ends the fixed-order sum of the
-// warps' partials.
+// operand layout once, then per stage the warp's share (an eighth or a
+// sixteenth) of the k range of one 16-row tile, and one stage after a tile
+// ends the fixed-order sum of the warps' partials.
 template <int QT, int NTL, bool X16, bool DOTS>
 __device__ __forceinline__ void consume(uint8_t* smem, const Plan& P, float* __restrict__ out,
                                         int32_t* __restrict__ dots, int od, int K, int nt, int stages, int t_begin,
