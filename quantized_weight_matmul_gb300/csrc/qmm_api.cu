@@ -78,27 +78,19 @@ int matmul_route(int qtype, int64_t nt, int64_t K) {
 }
 
 // Every refusal of the tensor-core route, checked before any device work is
-// enqueued; on success *status is the device status word.
-// The tensor-core route's own shape rule (host only), beyond check_shape:
-// none at present (rows of any pitch are staged, see qmm_gemm_tc.cu).
-int gemm_shape(int qtype, int64_t K) {
-  (void)qtype;
-  (void)K;
-  return QMM_OK;
-}
-
-int gemm_check(int qtype, int64_t od, int64_t K, int64_t nt, const void* ws, size_t ws_bytes, int** status) {
+// enqueued (the route takes any shape check_shape accepts: rows of any pitch
+// are staged); on success *status is the device status word.
+int gemm_check(int64_t od, int64_t K, int64_t nt, const void* ws, size_t ws_bytes, int** status) {
   if (ws_bytes < gemm_ws(od, K, nt)) return QMM_EWORKSPACE;
   if (!ws) return QMM_ENULL;
   if (!aligned16(ws)) return QMM_EALIGN;
-  if (int rc = gemm_shape(qtype, K)) return rc;
   return status_ptr(status);
 }
 
 int gemm_core(int qtype, const void* W, const int8_t* xq, const float* xds, float* out, int32_t* dots,
               int64_t od, int64_t K, int64_t nt, void* ws, size_t ws_bytes, bool prep, cudaStream_t st) {
   int* status = nullptr;
-  int rc = gemm_check(qtype, od, K, nt, ws, ws_bytes, &status);
+  int rc = gemm_check(od, K, nt, ws, ws_bytes, &status);
   if (rc) return rc;
   __half* xh = static_cast<__half*>(ws);
   float* scl = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + gemm_xh_bytes(nt, K));
@@ -201,9 +193,9 @@ int qmm_matmul(int qtype, const void* W, const float* x, int8_t* xq, float* xds,
   int rc = check_shape(od, K, nt);
   if (rc) return rc;
   if (!aligned16(W) || !aligned16(x) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
+  if (flags & ~(unsigned)QMM_FLAG_STATIC_WEIGHTS) return QMM_EINVAL_SHAPE;
   rc = check_device();
   if (rc) return rc;
-  if (flags & ~(unsigned)QMM_FLAG_STATIC_WEIGHTS) return QMM_EINVAL_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int path = matmul_route(qtype, nt, K);
   if (path == QMM_PATH_FUSED_MMVQ) {
@@ -222,7 +214,7 @@ int qmm_matmul(int qtype, const void* W, const float* x, int8_t* xq, float* xds,
     return launch_gemv(qtype, W, xq, xds, out, nullptr, od, K, nt, status, Dep::kPdlStaticW, st);
   }
   int* status = nullptr;
-  rc = gemm_check(qtype, od, K, nt, workspace, ws_bytes, &status);
+  rc = gemm_check(od, K, nt, workspace, ws_bytes, &status);
   if (rc) return rc;
   // the quantizer writes the tensor-core operands directly: no separate prepass
   __half* xh = static_cast<__half*>(workspace);
@@ -340,8 +332,6 @@ extern "C" int qmm_gemm_builtin_workspace(int qtype, const void* W, const int8_t
   if (!aligned16(W) || !aligned16(xq) || !aligned16(xds) || !aligned16(out)) return QMM_EALIGN;
   const size_t need = gemm_ws(od, K, nt);
   if (need > (size_t)QMM_BUILTIN_WORKSPACE_BYTES) return QMM_EWORKSPACE;
-  rc = gemm_shape(qtype, K);
-  if (rc) return rc;
   rc = check_device();
   if (rc) return rc;
   void* ws = nullptr;
@@ -350,7 +340,7 @@ extern "C" int qmm_gemm_builtin_workspace(int qtype, const void* W, const int8_t
   // every remaining refusal happens here, before the padding clears below
   // are enqueued: a refused call leaves the shared array untouched
   int* status = nullptr;
-  rc = gemm_check(qtype, od, K, nt, ws, (size_t)QMM_BUILTIN_WORKSPACE_BYTES, &status);
+  rc = gemm_check(od, K, nt, ws, (size_t)QMM_BUILTIN_WORKSPACE_BYTES, &status);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The prepass writes the scale planes only for tokens < nt; the padding

@@ -57,6 +57,37 @@ def test_argument_checks_need_no_device():
     assert qmm.qmm_debug_inject_stall(0, 0) == qmm.QMM_OK
 
 
+def test_every_entry_point_refuses_bad_arguments_first():
+    """Each compute entry point checks type, pointers, shape, alignment and
+    flags before it touches the device, so these refusals need no GPU."""
+    buf = ctypes.create_string_buffer(4096 + 16)
+    p = (ctypes.addressof(buf) + 15) & ~15
+    Q4, Q6 = qmm.Q4_K, qmm.Q6_K
+    # quantizer: pointers, shape (nt >= 1, K a multiple of 32), alignment
+    assert qmm.qmm_quantize_q8_1(0, 1, 64, p, p, 0) == qmm.QMM_ENULL
+    assert qmm.qmm_quantize_q8_1(p, 0, 64, p, p, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_quantize_q8_1(p + 4, 1, 64, p, p, 0) == qmm.QMM_EALIGN
+    assert qmm.qmm_quantize_q8_1(p, 1, 64, p, p + 8, 0) == qmm.QMM_EALIGN
+    # the whole path: type, pointers, shape, alignment, unknown flag bits
+    args = [p, p, p, p, p, 256, 256, 1, 0, 0]
+    assert qmm.qmm_matmul(3, *args, 0, 0) == qmm.QMM_EINVAL_QTYPE
+    assert qmm.qmm_matmul(Q4, p, 0, p, p, p, 256, 256, 1, 0, 0, 0, 0) == qmm.QMM_ENULL
+    assert qmm.qmm_matmul(Q6, p, p, p, p, p, 256, 300, 1, 0, 0, 0, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_matmul(Q4, p, p, p, p, p, 256, 256, 0, 0, 0, 0, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_matmul(Q4, p, p, p, p, p + 8, 256, 256, 1, 0, 0, 0, 0) == qmm.QMM_EALIGN
+    assert qmm.qmm_matmul(Q4, *args, 2, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_matmul(Q4, *args, 0xFFFFFFFE, 0) == qmm.QMM_EINVAL_SHAPE
+    # GEMM on caller-quantized input
+    assert qmm.qmm_gemm(9, p, p, p, p, 256, 256, 32, p, 4096, 0) == qmm.QMM_EINVAL_QTYPE
+    assert qmm.qmm_gemm(Q4, p, p, p, 0, 256, 256, 32, p, 4096, 0) == qmm.QMM_ENULL
+    assert qmm.qmm_gemm(Q6, p, p, p + 4, p, 256, 256, 32, p, 4096, 0) == qmm.QMM_EALIGN
+    # block-dot test hook
+    assert qmm.qmm_debug_block_dots(9, p, p, p, 256, 256, 1, p, 0, 0, 0, 0) == qmm.QMM_EINVAL_QTYPE
+    assert qmm.qmm_debug_block_dots(Q4, p, p, p, 256, 256, 1, 0, 0, 0, 0, 0) == qmm.QMM_ENULL
+    assert qmm.qmm_debug_block_dots(Q4, p, p, p, 256, 512 + 32, 1, p, 0, 0, 0, 0) == qmm.QMM_EINVAL_SHAPE
+    assert qmm.qmm_debug_block_dots(Q6, p + 2, p, p, 256, 256, 1, p, 0, 0, 0, 0) == qmm.QMM_EALIGN
+
+
 def test_valid_call_without_a_gpu_fails_loudly():
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
@@ -64,6 +95,9 @@ def test_valid_call_without_a_gpu_fails_loudly():
     buf = ctypes.create_string_buffer(4096 + 16)
     p = (ctypes.addressof(buf) + 15) & ~15
     assert qmm.qmm_gemv(qmm.Q4_K, p, p, p, p, 256, 256, 1, 0) == qmm.QMM_EDEVICE
+    assert qmm.qmm_matmul(qmm.Q4_K, p, p, p, p, p, 256, 256, 1, 0, 0, qmm.QMM_FLAG_STATIC_WEIGHTS, 0) == \
+        qmm.QMM_EDEVICE
+    assert qmm.qmm_quantize_q8_1(p, 1, 64, p, p, 0) == qmm.QMM_EDEVICE
 
 
 def test_strerror_covers_codes():
