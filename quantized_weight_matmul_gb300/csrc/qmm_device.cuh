@@ -23,28 +23,6 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
   return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xFFFFu)));
 }
 
-// The 6-bit (scale, min) pair of Q4_K sub-block j ("llama.cpp MMQ", sec. 6,
-// get_scale_min_k4) from the three header words that hold scales[0..11]
-// (words 1..3 of the 16-byte Q4_K header: bytes 4..15 of the block):
-// sub-blocks 0-3 keep both in the low 6 bits of bytes j and j+4; sub-blocks
-// 4-7 keep the low 4 bits in the two nibbles of byte j+4 and the top 2 bits
-// in the top of bytes j-4 and j.
-__device__ __forceinline__ void q4k_scale_min_words(uint32_t w0, uint32_t w1, uint32_t w2, int j,
-                                                    int& sc, int& m) {
-  // byte k of scales[] = byte (k%4) of word (k/4)
-  auto byte_of = [&](int k) -> int {
-    uint32_t w = k < 4 ? w0 : (k < 8 ? w1 : w2);
-    return (int)((w >> (8 * (k & 3))) & 0xFF);
-  };
-  if (j < 4) {
-    sc = byte_of(j) & 63;
-    m = byte_of(j + 4) & 63;
-  } else {
-    sc = (byte_of(j + 4) & 0x0F) | ((byte_of(j - 4) >> 6) << 4);
-    m = (byte_of(j + 4) >> 4) | ((byte_of(j) >> 6) << 4);
-  }
-}
-
 // The (scale, min) pairs of sub-blocks 2p and 2p+1 from the header
 // words holding scales[0..11] ("llama.cpp MMQ", sec. 6): sub-blocks 0-3 keep
 // both 6-bit codes in bytes j and j+4; sub-blocks 4-7 keep the low 4 bits in
@@ -171,21 +149,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait with a suspend-time hint: a thread whose phase is not complete is
-// parked by the hardware until it completes (or `ns` nanoseconds pass)
-// instead of returning at once to poll again, which keeps waiting warps off
-// the issue slots and shared-memory ports the working warps need.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, "
-      "p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Shared abort state of one CTA: a flag every wait polls, the device status
 // word, and the deadline after which a wait gives up.
 struct Guard {
@@ -203,20 +166,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Gu
     if (mbar_try_wait(bar, parity)) return true;
     if (*g.abort_flag) return false;
     if ((it & 63u) == 0 && global_ns() > g.deadline_ns) {
-      *g.abort_flag = 1;
-      report(g.status, QMM_ETIMEOUT);
-      return false;
-    }
-  }
-}
-
-// wait_bar whose polls park the thread for up to 20 us each (see
-// mbar_try_wait_sleep); the deadline is checked after every poll.
-__device__ __forceinline__ bool wait_bar_sleep(uint32_t bar, uint32_t parity, const Guard& g) {
-  for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if (*g.abort_flag) return false;
-    if (global_ns() > g.deadline_ns) {
       *g.abort_flag = 1;
       report(g.status, QMM_ETIMEOUT);
       return false;
@@ -442,13 +391,6 @@ __device__ __forceinline__ void tc_st_32x32_x32(uint32_t taddr, const uint32_t (
       "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
-__device__ __forceinline__ void tc_st_32x32_x16(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
-}
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -464,26 +406,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 // spill one of them in between, which reads it before the data has arrived
 // (wrong values in a few columns of one warp's load, more often under
 // register pressure).  Here the outputs exist only after the wait.
-// Two 32-column loads (at taddr0 and taddr1) with one wait.
-__device__ __forceinline__ void tc_ld_32x32_x2_sync(uint32_t taddr0, uint32_t taddr1, uint32_t (&v)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
-        "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]),
-        "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]),
-        "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
-        "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
-      : "r"(taddr0), "r"(taddr1)
-      : "memory");
-}
-
 __device__ __forceinline__ void tc_ld_32x32_sync(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
