@@ -12,7 +12,6 @@ from __future__ import annotations
 import numpy as np
 
 import oracle
-from quantized_weight_matmul_gb300 import synth
 
 REL_TOL = 1e-4
 _ORA = None
